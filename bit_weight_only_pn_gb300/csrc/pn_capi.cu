@@ -1,0 +1,228 @@
+// pn_capi.cu -- the C ABI declared in include/pn.h: argument checks, kernel choice, launches.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pn.h"
+#include "pn_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_cc_major[kMaxDevices];
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+
+int per_block(int type) { return type == PN_TYPE_PN3T ? 80 : (type == PN_TYPE_PN4T ? 64 : 0); }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+// SM count and compute-capability major of the current device (cached).
+pn_status device_info(int* sms, int* major) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return PN_ECUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return PN_EUNSUPPORTED;
+    int s = g_sm_count[dev].load(std::memory_order_relaxed);
+    int m = g_cc_major[dev].load(std::memory_order_relaxed);
+    if (s <= 0) {
+        if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&m, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return PN_ECUDA;
+        }
+        g_cc_major[dev].store(m, std::memory_order_relaxed);
+        g_sm_count[dev].store(s, std::memory_order_relaxed);
+    }
+    *sms = s;
+    *major = m;
+    return PN_OK;
+}
+
+// Shared checks of one GEMV operand set; fills `t`.
+pn_status check_tensor(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M,
+                       float* y, pn::GemvTensor* t) {
+    const int bpb = per_block(type);
+    if (bpb == 0 || K <= 0 || K % bpb != 0 || N < 0) return PN_EINVAL;
+    if (M < 1 || M > PN_MAX_M) return PN_EINVAL;
+    const int64_t nb = K / bpb;
+    if (N > INT32_MAX / 2 || nb > INT32_MAX / 8 || K > INT32_MAX / PN_MAX_M) return PN_EINVAL;
+    if (N > 0 && (!W || !x || !y)) return PN_EINVAL;
+    if (!aligned(W, 2) || !aligned(x, 2) || !aligned(y, 4)) return PN_EALIGN;
+    const size_t wbytes = static_cast<size_t>(N) * nb * PN_BLOCK_BYTES;
+    const size_t xbytes = static_cast<size_t>(M) * K * 2, ybytes = static_cast<size_t>(M) * N * 4;
+    if (N > 0 && (overlaps(y, ybytes, W, wbytes) || overlaps(y, ybytes, x, xbytes))) return PN_EINVAL;
+    t->W = static_cast<const uint8_t*>(W);
+    t->x = x;
+    t->y = y;
+    t->type = type;
+    t->N = static_cast<int>(N);
+    t->nb = static_cast<int>(nb);
+    return PN_OK;
+}
+
+bool tc_eligible(const pn::GemvTensor& t) {
+    return t.nb % 8 == 0 && aligned(t.W, 16) && aligned(t.x, 16);
+}
+
+pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t ws_bytes, int algo,
+                    cudaStream_t s) {
+    int sms = 0, major = 0;
+    pn_status st = device_info(&sms, &major);
+    if (st != PN_OK) return st;
+    if (algo != PN_ALGO_AUTO && algo != PN_ALGO_TENSOR_CORE && algo != PN_ALGO_CUDA_CORE) return PN_EINVAL;
+    pn::GemvTensor tc[pn::kMaxLayer];
+    pn::GemvTensor simt[pn::kMaxLayer];
+    int ntc = 0, nsimt = 0;
+    for (int e = 0; e < count; ++e) {
+        if (ts[e].N == 0) continue;
+        const bool ok_tc = tc_eligible(ts[e]) && major >= 10;
+        if (algo == PN_ALGO_TENSOR_CORE && !ok_tc) return major >= 10 ? PN_EALIGN : PN_EUNSUPPORTED;
+        if (algo != PN_ALGO_CUDA_CORE && ok_tc) tc[ntc++] = ts[e];
+        else simt[nsimt++] = ts[e];
+    }
+    if (ntc > 0) {
+        if (!ws || !aligned(ws, 256)) return PN_EINVAL;
+        int too_small = 0;
+        cudaError_t e = pn::launch_gemv_tc(tc, ntc, M, ws, ws_bytes, sms, g_timeout_ns.load(), s, &too_small);
+        if (too_small) return PN_EINVAL;
+        if (e != cudaSuccess) return PN_ECUDA;
+    }
+    for (int i = 0; i < nsimt; ++i)
+        if (pn::launch_gemv_simt(simt[i], M, s) != cudaSuccess) return PN_ECUDA;
+    return PN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pn_abi_version(void) { return 1; }
+
+const char* pn_status_string(pn_status s) {
+    switch (s) {
+        case PN_OK: return "ok";
+        case PN_EINVAL: return "invalid argument";
+        case PN_EALIGN: return "misaligned pointer";
+        case PN_EUNSUPPORTED: return "unsupported on this device or build";
+        case PN_ECUDA: return "CUDA error";
+        case PN_ETIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+int pn_weights_per_block(int type) { return per_block(type); }
+
+size_t pn_row_bytes(int type, int64_t K) {
+    const int bpb = per_block(type);
+    if (bpb == 0 || K <= 0 || K % bpb != 0) return 0;
+    return static_cast<size_t>(K / bpb) * PN_BLOCK_BYTES;
+}
+
+pn_status pn_pack(int type, const float* w, int64_t N, int64_t K, void* W, pn_stream stream) {
+    const int bpb = per_block(type);
+    if (bpb == 0 || K <= 0 || K % bpb != 0 || N < 0) return PN_EINVAL;
+    if (N == 0) return PN_OK;
+    if (!w || !W) return PN_EINVAL;
+    if (!aligned(w, 4) || !aligned(W, 2)) return PN_EALIGN;
+    if (overlaps(w, static_cast<size_t>(N) * K * 4, W, static_cast<size_t>(N) * (K / bpb) * PN_BLOCK_BYTES))
+        return PN_EINVAL;
+    return pn::launch_pack(type, w, N, K / bpb, W, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PN_OK : PN_ECUDA;
+}
+
+pn_status pn_unpack(int type, const void* W, int64_t N, int64_t K, float* w, pn_stream stream) {
+    const int bpb = per_block(type);
+    if (bpb == 0 || K <= 0 || K % bpb != 0 || N < 0) return PN_EINVAL;
+    if (N == 0) return PN_OK;
+    if (!w || !W) return PN_EINVAL;
+    if (!aligned(w, 4) || !aligned(W, 2)) return PN_EALIGN;
+    if (overlaps(w, static_cast<size_t>(N) * K * 4, W, static_cast<size_t>(N) * (K / bpb) * PN_BLOCK_BYTES))
+        return PN_EINVAL;
+    return pn::launch_unpack(type, W, N, K / bpb, w, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PN_OK : PN_ECUDA;
+}
+
+size_t pn_workspace_bytes(int64_t total_rows) {
+    int sms = 0, major = 0;
+    if (total_rows < 0 || device_info(&sms, &major) != PN_OK) return 0;
+    const int64_t tiles = (total_rows + 15) / 16 + pn::kMaxLayer;
+    return pn::workspace_layout(tiles, pn::tc_max_ctas(sms)).total;
+}
+
+pn_status pn_workspace_init(void* workspace, size_t workspace_bytes, pn_stream stream) {
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return PN_EINVAL;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PN_OK : PN_ECUDA;
+}
+
+pn_status pn_workspace_status(void* workspace, size_t workspace_bytes, pn_stream stream) {
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return PN_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return PN_ECUDA;
+    }
+    if (word == 0) return PN_OK;
+    if (cudaMemset(workspace, 0, workspace_bytes) != cudaSuccess) { cudaGetLastError(); return PN_ECUDA; }
+    return word == PN_ETIMEOUT ? PN_ETIMEOUT : PN_ECUDA;
+}
+
+pn_status pn_gemv_ex(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M,
+                     float* y, void* workspace, size_t workspace_bytes, int algo, pn_stream stream) {
+    pn::GemvTensor t{};
+    pn_status st = check_tensor(type, W, N, K, x, M, y, &t);
+    if (st != PN_OK) return st;
+    if (N == 0) return PN_OK;
+    return run_layer(&t, 1, M, workspace, workspace_bytes, algo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pn_status pn_gemv(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M,
+                  float* y, void* workspace, size_t workspace_bytes, pn_stream stream) {
+    return pn_gemv_ex(type, W, N, K, x, M, y, workspace, workspace_bytes, PN_ALGO_AUTO, stream);
+}
+
+pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* workspace,
+                           size_t workspace_bytes, int algo, pn_stream stream) {
+    if (!descs || count < 1 || count > PN_MAX_LAYER) return PN_EINVAL;
+    pn::GemvTensor ts[pn::kMaxLayer];
+    for (int e = 0; e < count; ++e) {
+        const pn_gemv_desc& d = descs[e];
+        pn_status st = check_tensor(d.type, d.W, d.N, d.K, d.x, M, d.y, &ts[e]);
+        if (st != PN_OK) return st;
+    }
+    // No output may overlap another entry's operands or output.
+    for (int a = 0; a < count; ++a) {
+        if (descs[a].N == 0) continue;
+        const size_t ya = static_cast<size_t>(M) * descs[a].N * 4;
+        for (int b = 0; b < count; ++b) {
+            if (b == a || descs[b].N == 0) continue;
+            const int bpb = per_block(descs[b].type);
+            const size_t wb = static_cast<size_t>(descs[b].N) * (descs[b].K / bpb) * PN_BLOCK_BYTES;
+            const size_t xb = static_cast<size_t>(M) * descs[b].K * 2;
+            const size_t yb = static_cast<size_t>(M) * descs[b].N * 4;
+            if (overlaps(descs[a].y, ya, descs[b].W, wb) || overlaps(descs[a].y, ya, descs[b].x, xb) ||
+                overlaps(descs[a].y, ya, descs[b].y, yb))
+                return PN_EINVAL;
+        }
+    }
+    return run_layer(ts, count, M, workspace, workspace_bytes, algo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pn_status pn_gemv_layer(const pn_gemv_desc* descs, int count, int M, void* workspace,
+                        size_t workspace_bytes, pn_stream stream) {
+    return pn_gemv_layer_ex(descs, count, M, workspace, workspace_bytes, PN_ALGO_AUTO, stream);
+}
+
+void pn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
+
+}  // extern "C"

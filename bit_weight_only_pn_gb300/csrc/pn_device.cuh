@@ -1,0 +1,184 @@
+// pn_device.cuh -- PN format constants and the sm_103a PTX helpers used by the kernels.
+//
+// Format (tensorless docs, "Why a P100-native weight format"): a 34-byte block
+// holds an fp16 scale d followed by eight 32-bit code words; pn3t packs ten
+// 3-bit codes per word (80 weights per block), pn4t eight 4-bit codes (64).
+// Even codes sit in bits 0..15 and odd codes in bits 16..31 at the same offsets
+// ("Codes never straddle the two halves of a word"); a weight is d * (n - z)
+// ("Exact decode in fp32") with mid-tread zero point z = 4 (pn3t) / 8 (pn4t).
+// Layout readings: d in bytes 0..1, word j in bytes 2+4j..5+4j, weight k is code
+// k % cpw of word k / cpw, code c at bit 16*(c&1) + bits*(c>>1).
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace pn {
+
+constexpr int kBlockBytes = 34;
+constexpr int kWordsPerBlock = 8;
+constexpr int kPn3t = 124;
+constexpr int kPn4t = 125;
+
+template <int TYPE> struct Format;
+
+template <> struct Format<kPn3t> {
+    static constexpr int kPerBlock = 80;   // weights per block
+    static constexpr int kPerWord = 10;    // codes per word
+    static constexpr int kBits = 3;
+    static constexpr int kZero = 4;
+    static constexpr int kPairs = 5;       // half2 code pairs per word
+    // Upper code pairs are shifted down by this much so that every pair's two
+    // codes sit inside the 10-bit mantissa of an fp16 (see decode_pair).
+    static constexpr int kHighShift = 9;
+    static constexpr int kLowPairs = 3;    // pairs 0..2 decode from the unshifted word
+};
+
+template <> struct Format<kPn4t> {
+    static constexpr int kPerBlock = 64;
+    static constexpr int kPerWord = 8;
+    static constexpr int kBits = 4;
+    static constexpr int kZero = 8;
+    static constexpr int kPairs = 4;
+    static constexpr int kHighShift = 8;
+    static constexpr int kLowPairs = 2;
+};
+
+__host__ __device__ constexpr int per_block(int type) { return type == kPn3t ? 80 : 64; }
+
+// ------------------------------------------------------------- PTX helpers --
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// One probe of phase `parity` of the barrier; true once that phase has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Bulk copy (TMA engine, no tensor map) of `bytes` (multiple of 16, both
+// addresses 16-byte aligned) from global to this CTA's shared memory; the
+// byte count is credited to the transaction count of `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds_u64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint4 lds_u128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
+// (a & b) | c in one LOP3.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Bytes {a.hi, b.lo}: the 32-bit word that starts two bytes into `a`.
+__device__ __forceinline__ uint32_t realign16(uint32_t a, uint32_t b) {
+    return __byte_perm(a, b, 0x5432);
+}
+
+// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1, const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1),
+          "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// ----------------------------------------------------------- code decoding --
+//
+// decode_pair<TYPE, P>(word, shifted) returns the half2 (n_{2P} - z, n_{2P+1} - z)
+// of code pair P of a word, exactly.  A LOP3 keeps the pair's two codes (one
+// per 16-bit half, same offset) and ORs in the fp16 bit pattern 0x6400 (1024.0),
+// giving the halves 1024 + n * 2^off as long as the code lies in the 10-bit
+// mantissa; one fma.rn.f16x2 by 2^-off minus (1024 * 2^-off + z) leaves n - z.
+// Every intermediate value is an fp16 number, so the result is exact.  Pairs
+// whose offset would reach the exponent bits use the word shifted right once.
+
+template <int TYPE, int P>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t word, uint32_t shifted) {
+    using F = Format<TYPE>;
+    constexpr bool kHigh = P >= F::kLowPairs;
+    constexpr int kOff = F::kBits * (kHigh ? P - F::kLowPairs : P);
+    constexpr uint32_t kMask = ((1u << F::kBits) - 1u) << kOff;
+    constexpr uint32_t kMask2 = kMask | (kMask << 16);
+    // scale 2^-off as fp16 (exponent 15 - off), replicated into both halves
+    constexpr uint32_t kScale = static_cast<uint32_t>(15 - kOff) << 10;
+    constexpr uint32_t kScale2 = kScale | (kScale << 16);
+    // bias -(1024 * 2^-off + z) as fp16
+    constexpr uint32_t kBias = (TYPE == kPn3t)
+        ? (kOff == 0 ? 0xE404u : kOff == 3 ? 0xD820u : 0xCD00u)   // -1028, -132, -20
+        : (kOff == 0 ? 0xE408u : 0xD480u);                         // -1032, -72
+    constexpr uint32_t kBias2 = kBias | (kBias << 16);
+    return hfma2(and_or(kHigh ? shifted : word, kMask2, 0x64006400u), kScale2, kBias2);
+}
+
+}  // namespace pn

@@ -1,0 +1,198 @@
+"""Python binding of the PN CUDA library (include/pn.h): argument marshalling only.
+
+PyTorch supplies device memory and the current CUDA stream; every step of the
+computation runs in the library's kernels.  There is no CPU path: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PN3T = 124
+PN4T = 125
+ALGO_AUTO, ALGO_TENSOR_CORE, ALGO_CUDA_CORE = 0, 1, 2
+MAX_M = 8
+MAX_LAYER = 8
+STATUS = {0: "PN_OK", 1: "PN_EINVAL", 2: "PN_EALIGN", 3: "PN_EUNSUPPORTED", 4: "PN_ECUDA",
+          5: "PN_ETIMEOUT"}
+
+LIBRARY = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpn_gb300.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("type", ctypes.c_int), ("W", ctypes.c_void_p), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY):
+                raise RuntimeError(f"PN CUDA library not built ({LIBRARY}); run "
+                                   "`python -m bit_weight_only_pn_gb300.build`")
+            L = ctypes.CDLL(LIBRARY)
+            vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+            L.pn_abi_version.restype = i32
+            L.pn_status_string.restype = ctypes.c_char_p
+            L.pn_status_string.argtypes = [i32]
+            L.pn_weights_per_block.restype = i32
+            L.pn_weights_per_block.argtypes = [i32]
+            L.pn_row_bytes.restype = sz
+            L.pn_row_bytes.argtypes = [i32, i64]
+            L.pn_pack.restype = i32
+            L.pn_pack.argtypes = [i32, vp, i64, i64, vp, vp]
+            L.pn_unpack.restype = i32
+            L.pn_unpack.argtypes = [i32, vp, i64, i64, vp, vp]
+            L.pn_workspace_bytes.restype = sz
+            L.pn_workspace_bytes.argtypes = [i64]
+            L.pn_workspace_init.restype = i32
+            L.pn_workspace_init.argtypes = [vp, sz, vp]
+            L.pn_workspace_status.restype = i32
+            L.pn_workspace_status.argtypes = [vp, sz, vp]
+            L.pn_gemv.restype = i32
+            L.pn_gemv.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp, sz, vp]
+            L.pn_gemv_ex.restype = i32
+            L.pn_gemv_ex.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp, sz, i32, vp]
+            L.pn_gemv_layer.restype = i32
+            L.pn_gemv_layer.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, vp]
+            L.pn_gemv_layer_ex.restype = i32
+            L.pn_gemv_layer_ex.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, i32, vp]
+            L.pn_set_wait_timeout_ns.restype = None
+            L.pn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+            _lib = L
+        return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise PnError(status, what)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _require(t: torch.Tensor, dtype, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def weights_per_block(pn_type: int) -> int:
+    return int(lib().pn_weights_per_block(pn_type))
+
+
+def row_bytes(pn_type: int, K: int) -> int:
+    return int(lib().pn_row_bytes(pn_type, K))
+
+
+def pack(pn_type: int, w: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 weights [N][K] -> PN rows uint8 [N][row_bytes]."""
+    _require(w, torch.float32, "w")
+    N, K = w.shape
+    rb = row_bytes(pn_type, K)
+    if rb == 0:
+        raise ValueError(f"K={K} is not a whole number of blocks")
+    if out is None:
+        out = torch.empty((N, rb), dtype=torch.uint8, device=w.device)
+    _require(out, torch.uint8, "out")
+    _check(lib().pn_pack(pn_type, _ptr(w), N, K, _ptr(out), _stream(stream)), "pn_pack")
+    return out
+
+
+def unpack(pn_type: int, W: torch.Tensor, K: int, out: torch.Tensor | None = None,
+           stream=None) -> torch.Tensor:
+    """PN rows uint8 [N][row_bytes] -> fp32 weights [N][K] (exact)."""
+    _require(W, torch.uint8, "W")
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=W.device)
+    _require(out, torch.float32, "out")
+    _check(lib().pn_unpack(pn_type, _ptr(W), N, K, _ptr(out), _stream(stream)), "pn_unpack")
+    return out
+
+
+class Workspace:
+    """Zeroed device scratch for GEMV calls on one device (see pn_workspace_bytes)."""
+
+    def __init__(self, total_rows: int, device=None, stream=None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        with torch.cuda.device(self.device):
+            self.nbytes = int(lib().pn_workspace_bytes(int(total_rows)))
+            if self.nbytes == 0:
+                raise PnError(4, "pn_workspace_bytes")
+            self.buffer = torch.zeros(self.nbytes, dtype=torch.uint8, device=self.device)
+        self.total_rows = int(total_rows)
+
+    @property
+    def ptr(self) -> int:
+        return self.buffer.data_ptr()
+
+    def status(self, stream=None) -> int:
+        """Synchronise, read and clear the device status word (0 = ok)."""
+        return int(lib().pn_workspace_status(self.ptr, self.nbytes, _stream(stream)))
+
+
+def gemv(pn_type: int, W: torch.Tensor, K: int, x: torch.Tensor, y: torch.Tensor | None = None,
+         workspace: Workspace | None = None, algo: int = ALGO_AUTO, stream=None) -> torch.Tensor:
+    """y[M][N] = decode(W)[N][K] @ x[M][K]^T with fp32 accumulation (1 <= M <= 8)."""
+    _require(W, torch.uint8, "W")
+    _require(x, torch.float16, "x")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    M = x.shape[0]
+    N = W.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=W.device)
+    _require(y, torch.float32, "y")
+    ws_ptr, ws_bytes = (workspace.ptr, workspace.nbytes) if workspace is not None else (None, 0)
+    _check(lib().pn_gemv_ex(pn_type, _ptr(W), N, K, _ptr(x), M, _ptr(y), ws_ptr, ws_bytes, algo,
+                            _stream(stream)), "pn_gemv")
+    return y
+
+
+def gemv_layer(entries, M: int, workspace: Workspace | None = None, algo: int = ALGO_AUTO,
+               stream=None):
+    """Several independent GEMVs in one launch.
+
+    ``entries`` is a sequence of (pn_type, W, K, x, y) with x fp16 [M][K] and y
+    fp32 [M][N] preallocated.  Returns the list of y tensors.
+    """
+    entries = list(entries)
+    arr = (_Desc * len(entries))()
+    for i, (t, W, K, x, y) in enumerate(entries):
+        _require(W, torch.uint8, "W")
+        _require(x, torch.float16, "x")
+        _require(y, torch.float32, "y")
+        arr[i] = _Desc(t, _ptr(W), W.shape[0], K, _ptr(x), _ptr(y))
+    ws_ptr, ws_bytes = (workspace.ptr, workspace.nbytes) if workspace is not None else (None, 0)
+    _check(lib().pn_gemv_layer_ex(arr, len(entries), M, ws_ptr, ws_bytes, algo, _stream(stream)),
+           "pn_gemv_layer")
+    return [e[4] for e in entries]
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib().pn_set_wait_timeout_ns(int(ns))

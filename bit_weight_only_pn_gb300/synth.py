@@ -23,6 +23,9 @@ K = 6144 and 17408 for pn4t):
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 _G = np.uint64(0x9E3779B97F4A7C15)
@@ -51,11 +54,36 @@ def uniform(seed: int, count: int, start: int = 0) -> np.ndarray:
     return (splitmix64(seed, count, start) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
 
 
-def normal(seed: int, count: int) -> np.ndarray:
-    """Standard normal fp64 samples (Box-Muller, cosine branch)."""
-    u = uniform(seed, 2 * count)
-    u0, u1 = u[0::2], u[1::2]
-    return np.sqrt(-2.0 * np.log1p(-u0)) * np.cos(2.0 * np.pi * u1)
+_CHUNK = 1 << 22
+
+
+def normal(seed: int, count: int, start: int = 0) -> np.ndarray:
+    """Standard normal fp64 samples ``start .. start+count-1`` (Box-Muller, cosine branch)."""
+    out = np.empty(count, dtype=np.float64)
+    for lo in range(0, count, _CHUNK):
+        n = min(_CHUNK, count - lo)
+        u = uniform(seed, 2 * n, 2 * (start + lo))
+        out[lo:lo + n] = np.sqrt(-2.0 * np.log1p(-u[0::2])) * np.cos(2.0 * np.pi * u[1::2])
+    return out
+
+
+def _normal_f32(seed: int, count: int, scale: float) -> np.ndarray:
+    """``scale * normal`` rounded to fp32; chunks run on a thread pool (numpy
+    releases the GIL inside its loops), each chunk drawing its own counters."""
+    out = np.empty(count, dtype=np.float32)
+
+    def fill(lo):
+        n = min(_CHUNK, count - lo)
+        out[lo:lo + n] = scale * normal(seed, n, lo)
+
+    starts = range(0, count, _CHUNK)
+    if count <= _CHUNK:
+        for lo in starts:
+            fill(lo)
+    else:
+        with ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as pool:
+            list(pool.map(fill, starts))
+    return out
 
 
 def weight_seed(config: int, tensor: int) -> int:
@@ -68,12 +96,23 @@ def x_seed(config: int, tensor: int) -> int:
 
 def weights(seed: int, n: int, k: int, std: float = 0.02) -> np.ndarray:
     """fp32 weights [n][k], ``std * normal``."""
-    return (std * normal(seed, n * k)).astype(np.float32).reshape(n, k)
+    return _normal_f32(seed, n * k, std).reshape(n, k)
 
 
 def activations(seed: int, m: int, k: int) -> np.ndarray:
     """fp16 activations [m][k] (RNE of a standard normal), returned as float16."""
     return normal(seed, m * k).astype(np.float16).reshape(m, k)
+
+
+def weight_rows(seed: int, n: int, k: int, rows, std: float = 0.02) -> np.ndarray:
+    """Rows ``rows`` of ``weights(seed, n, k, std)``, drawn without the other rows."""
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, k), dtype=np.float32)
+    for i, r in enumerate(rows):
+        if not 0 <= r < n:
+            raise IndexError(r)
+        out[i] = std * normal(seed, k, int(r) * k)
+    return out
 
 
 # The workloads: (type, K, N) per tensor.

@@ -1,0 +1,182 @@
+/*
+ * pn.h -- C ABI of the PN weight-only decode GEMV library for GB300 (sm_103a).
+ *
+ * The PN formats come from the tensorless documentation, page "Why a P100-native
+ * weight format":
+ *   - "Every block is 34 bytes": a block is a 2-byte fp16 scale d and eight
+ *     32-bit code words; pn3t holds 80 weights (ten 3-bit codes per word,
+ *     3.40 bits/weight), pn4t holds 64 weights (eight 4-bit codes per word,
+ *     4.25 bits/weight).  A row holds a whole number of blocks.
+ *   - "Codes never straddle the two halves of a word": even codes fill bits
+ *     0..15, odd codes bits 16..31, at the same offsets.
+ *   - "Exact decode in fp32": weight = d * (n - z), exact in fp32.
+ *   - "Zero is a code, and the scale has a sign": mid-tread codes, z = 4 for
+ *     pn3t (steps -4..+3); the signed scale puts the extra step on the side of
+ *     the block's largest weight.
+ *
+ * Where the page leaves the layout open this library reads it as follows (the
+ * same readings as the CPU oracle used by the tests):
+ *   - block bytes 0..1 = d (IEEE binary16, little-endian), bytes 2..33 = code
+ *     words w0..w7 (little-endian);
+ *   - weight k of a block is code c = k % cpw of word k / cpw (cpw = 10 pn3t,
+ *     8 pn4t); code c sits in half (c & 1) at bit offset bits * (c >> 1);
+ *     pn3t bits 15 and 31 are written as 0 and ignored on decode;
+ *   - z = 4 (pn3t) and z = 8 (pn4t, steps -8..+7);
+ *   - the packer rounds to nearest with d = fp16(a / -z), a = the block's
+ *     largest-magnitude weight (first on ties); codes n = clamp(rint(v / d),
+ *     -z, z-1) + z (fp32 divides, ties to even); a block whose scale is 0 or
+ *     underflows fp16 is the zero block (d = +0, all codes z); a scale above
+ *     the fp16 range saturates to +-65504.
+ *
+ * Layouts.  W: N rows of pn_row_bytes(type, K) bytes, row-major, no padding.
+ * Dense weights w: fp32 [N][K] row-major.  Activations x: IEEE binary16 bit
+ * patterns [M][K] row-major.  Outputs y: fp32 [M][N] row-major.
+ *
+ * Conventions.  Every pointer except descriptor arrays is device memory owned
+ * by the caller; the library allocates nothing.  Every call is asynchronous on
+ * the given CUDA stream (NULL = the legacy default stream) and returns after
+ * the launch.  Arguments are checked on the host before anything is launched;
+ * a failed check returns an error status and launches nothing.  A CUDA launch
+ * error is returned as PN_ECUDA.  No call aborts, throws or prints.
+ *
+ * Thread safety: calls may be made from several host threads; calls that share
+ * a workspace must be ordered on one stream.
+ */
+#ifndef PN_H
+#define PN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                      /* == cudaStream_t / CUstream */
+typedef struct CUstream_st* pn_stream;
+
+/* Weight types; the values are the GGUF type ids the page gives for PN
+ * ("Why the format is specific to this engine": 124 and 125). */
+typedef enum { PN_TYPE_PN3T = 124, PN_TYPE_PN4T = 125 } pn_type;
+
+typedef enum {
+    PN_OK = 0,
+    PN_EINVAL = 1,        /* bad type, size, count, null pointer, small workspace */
+    PN_EALIGN = 2,        /* a pointer is not aligned as documented */
+    PN_EUNSUPPORTED = 3,  /* valid request this build cannot serve (e.g. not sm_10x) */
+    PN_ECUDA = 4,         /* a CUDA runtime call or launch failed */
+    PN_ETIMEOUT = 5       /* a device-side wait gave up (reported by pn_workspace_status) */
+} pn_status;
+
+/* GEMV algorithm selection for pn_gemv_ex / pn_gemv_layer_ex. */
+typedef enum {
+    PN_ALGO_AUTO = 0,         /* tensor-core kernel where eligible, else CUDA cores */
+    PN_ALGO_TENSOR_CORE = 1,  /* TMA-staged rows, decode into mma.sync fragments   */
+    PN_ALGO_CUDA_CORE = 2     /* one lane per code word, fp32 FMAs                 */
+} pn_algo;
+
+#define PN_BLOCK_BYTES 34
+#define PN_MAX_M 8            /* largest activation count M per GEMV */
+#define PN_MAX_LAYER 8        /* most tensors per pn_gemv_layer call */
+
+/* Version of this ABI (incremented on any incompatible change). */
+int pn_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* pn_status_string(pn_status s);
+
+/* Weights per block (80 / 64) or 0 for an unknown type. */
+int pn_weights_per_block(int type);
+
+/* Bytes per PN row: (K / weights_per_block) * 34, or 0 if the type is unknown
+ * or K is not a positive multiple of the block size ("A row must hold a whole
+ * number of blocks"). */
+size_t pn_row_bytes(int type, int64_t K);
+
+/*
+ * pn_pack: quantise fp32 weights w [N][K] into PN rows W [N][row_bytes] with
+ * the signed-scale round-to-nearest rule above.  w must be 4-byte aligned, W
+ * 2-byte aligned; inputs must be finite (the result for non-finite inputs is
+ * unspecified).  Deterministic and byte-identical to the CPU oracle.
+ */
+pn_status pn_pack(int type, const float* w, int64_t N, int64_t K, void* W, pn_stream stream);
+
+/*
+ * pn_unpack: decode PN rows W [N][row_bytes] into fp32 w [N][K]; each weight is
+ * the single IEEE fp32 product d * (n - z), exact ("Exact decode in fp32"),
+ * including the sign of zero.  W 2-byte aligned, w 4-byte aligned.
+ */
+pn_status pn_unpack(int type, const void* W, int64_t N, int64_t K, float* w, pn_stream stream);
+
+/*
+ * Workspace for the GEMV calls.  The tensor-core kernel splits rows and K
+ * blocks evenly over the SMs; a tile whose K range is split between thread
+ * blocks is summed by the last contributor in a fixed order, so results are
+ * deterministic.  That needs device scratch: a status word, one counter per
+ * 16-row tile, and two partial-sum slots per thread block.
+ *
+ * pn_workspace_bytes(total_rows): bytes needed by one call whose tensors have
+ * total_rows rows in all (sum of N), on the current device.
+ * pn_workspace_init: zero a workspace (required once before first use; every
+ * call that completes leaves it zeroed again).
+ * pn_workspace_status: synchronise `stream`, read and clear the device status
+ * word of the workspace; returns PN_OK or the device-side error (PN_ETIMEOUT),
+ * and re-zeroes the whole workspace after an error.
+ * Workspace pointers must be 256-byte aligned.
+ */
+size_t pn_workspace_bytes(int64_t total_rows);
+pn_status pn_workspace_init(void* workspace, size_t workspace_bytes, pn_stream stream);
+pn_status pn_workspace_status(void* workspace, size_t workspace_bytes, pn_stream stream);
+
+/*
+ * pn_gemv: y[m][r] = sum_k w[r][k] * x[m][k] for m < M (1 <= M <= 8), r < N,
+ * where w is W decoded as in pn_unpack.  This is the decode GEMV of token
+ * generation (M = 1) and its skinny verification batch (M <= 8, one token plus
+ * drafts).  Products are exact in fp32 and sums are kept in fp32; every output
+ * is within 1e-5 * sum_k |w[r][k] x[m][k]| + 1e-6 of the exact value.
+ * Alignment: W and x 16-byte aligned for the tensor-core kernel (otherwise
+ * PN_ALGO_AUTO uses the CUDA-core kernel, which needs W and x 2-byte and y
+ * 4-byte aligned).  y must not overlap W or x.
+ */
+pn_status pn_gemv(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M,
+                  float* y, void* workspace, size_t workspace_bytes, pn_stream stream);
+
+pn_status pn_gemv_ex(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M,
+                     float* y, void* workspace, size_t workspace_bytes, int algo,
+                     pn_stream stream);
+
+/*
+ * pn_gemv_layer: the GEMVs of several independent tensors (one decoder layer's
+ * projections) in one launch, all with the same M.  The thread blocks share
+ * out the rows and K blocks of every tensor in proportion to their bytes.
+ * Descriptors are read on the host during the call.  No entry's y may overlap
+ * any entry's W, x or y.  At most PN_MAX_LAYER entries.
+ */
+typedef struct {
+    int type;               /* PN_TYPE_PN3T or PN_TYPE_PN4T            */
+    const void* W;          /* device, [N][pn_row_bytes(type, K)]      */
+    int64_t N;              /* rows                                    */
+    int64_t K;              /* input width                             */
+    const uint16_t* x;      /* device, fp16 [M][K]                     */
+    float* y;               /* device, fp32 [M][N]                     */
+} pn_gemv_desc;
+
+pn_status pn_gemv_layer(const pn_gemv_desc* descs, int count, int M, void* workspace,
+                        size_t workspace_bytes, pn_stream stream);
+
+pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* workspace,
+                           size_t workspace_bytes, int algo, pn_stream stream);
+
+/*
+ * Testing aid: the time limit, in nanoseconds, of every device-side wait in
+ * the tensor-core kernel (default 1e9).  A wait that runs out stops its thread
+ * block, which records PN_ETIMEOUT in the workspace status word and returns
+ * after its outstanding copies land.  Process-wide; not for concurrent use.
+ */
+void pn_set_wait_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PN_H */

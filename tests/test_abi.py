@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads and exports every symbol include/pn.h declares.
+
+These run without a GPU: only calls that return before touching the device
+(sizes, status strings, argument checks) are made.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_weight_only_pn_gb300 import build, pn
+    build.build()
+    return pn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(pn_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(n for n in names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "pn_gemv" in names and "pn_gemv_layer" in names and "pn_pack" in names
+    for name in names:
+        assert hasattr(lib, name), f"{name} missing from the library"
+
+
+def test_host_only_queries(lib):
+    assert lib.pn_abi_version() == 1
+    assert lib.pn_weights_per_block(124) == 80 and lib.pn_weights_per_block(125) == 64
+    assert lib.pn_weights_per_block(3) == 0
+    assert lib.pn_row_bytes(124, 5120) == 2176 and lib.pn_row_bytes(125, 17408) == 9248
+    assert lib.pn_row_bytes(124, 6144) == 0 and lib.pn_row_bytes(125, 0) == 0
+    assert lib.pn_row_bytes(125, -64) == 0
+    for s in range(6):
+        assert lib.pn_status_string(s)
+    assert lib.pn_status_string(99) == b"unknown status"
+
+
+PN_EINVAL, PN_EALIGN = 1, 2
+FAKE = 0x10000      # a 64 KiB-aligned address that is never dereferenced: checks fail first
+
+
+def test_argument_checks_return_before_any_launch(lib):
+    g = lib.pn_gemv_ex
+    # unknown type, K not a whole number of blocks, M out of range, negative N
+    assert g(7, FAKE, 16, 5120, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
+    assert g(124, FAKE, 16, 5121, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
+    assert g(124, FAKE, 16, 5120, FAKE * 2, 0, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
+    assert g(124, FAKE, 16, 5120, FAKE * 2, 9, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
+    assert g(124, FAKE, -1, 5120, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
+    # null pointers, misaligned pointers
+    assert g(124, None, 16, 5120, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
+    assert g(124, FAKE + 1, 16, 5120, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EALIGN
+    assert g(124, FAKE, 16, 5120, FAKE * 2 + 1, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EALIGN
+    assert g(124, FAKE, 16, 5120, FAKE * 2, 1, FAKE * 4 + 2, FAKE * 8, 1 << 20, 0, None) == PN_EALIGN
+    # y overlapping W or x
+    assert g(124, FAKE, 16, 5120, FAKE * 2, 1, FAKE + 64, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
+    # N = 0 is a no-op
+    assert g(124, FAKE, 0, 5120, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == 0
+    # pack / unpack checks
+    assert lib.pn_pack(124, FAKE, 4, 100, FAKE * 2, None) == PN_EINVAL
+    assert lib.pn_pack(124, FAKE + 2, 4, 80, FAKE * 2, None) == PN_EALIGN
+    assert lib.pn_unpack(125, FAKE * 2 + 1, 4, 64, FAKE, None) == PN_EALIGN
+    assert lib.pn_unpack(125, FAKE, 4, 64, FAKE + 8, None) == PN_EINVAL   # overlap
+    assert lib.pn_pack(125, FAKE, 0, 64, FAKE * 2, None) == 0
+    # workspace helpers
+    assert lib.pn_workspace_init(None, 1024, None) == PN_EINVAL
+    assert lib.pn_workspace_init(FAKE + 16, 1024, None) == PN_EINVAL
+
+
+def test_layer_checks(lib):
+    from bit_weight_only_pn_gb300.pn import _Desc
+    arr = (_Desc * 2)()
+    arr[0] = _Desc(124, FAKE, 32, 5120, FAKE * 2, FAKE * 4)
+    arr[1] = _Desc(125, FAKE * 8, 32, 6144, FAKE * 16, FAKE * 4 + 64)    # y overlaps entry 0's y
+    assert lib.pn_gemv_layer(arr, 2, 1, FAKE * 32, 1 << 20, None) == PN_EINVAL
+    assert lib.pn_gemv_layer(arr, 0, 1, FAKE * 32, 1 << 20, None) == PN_EINVAL
+    assert lib.pn_gemv_layer(arr, 9, 1, FAKE * 32, 1 << 20, None) == PN_EINVAL
+    assert lib.pn_gemv_layer(None, 1, 1, FAKE * 32, 1 << 20, None) == PN_EINVAL
