@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Benchmark of the PN decode GEMV on GB300; prints one JSON line.
+
+Workload (default): pn3t GEMV, N = 17408 rows, K = 5120 (64 blocks of 34 bytes
+per row, 37,879,808 bytes of packed weights), M = 1, fp16 x, fp32 y -- the
+FFN gate/up shape of a 27B-class model at the tensorless pages' widths.  A
+step is one GEMV over one batch (one token's x).  Other workloads:
+``--config 0|2|3|4`` (3/4: one decoder layer's seven GEMVs in one fused call at
+M = 1 / M = 8).
+
+Timing: weights are resident in HBM; eight copies (more than twice the 129 MB
+L2) are rotated so every step reads its weights from HBM.  Steps are captured
+in a CUDA graph (launch overhead would otherwise exceed a 6 us kernel) and
+timed with CUDA events on the launching stream, after a barrier and a
+synchronize on both sides; the max over ranks is taken.  ``value`` is the
+effective bandwidth: algorithmic bytes per GEMV (packed weights + x + y) over
+the time per GEMV.  ``e2e`` times the same GEMV through the public Python API
+with x copied from pinned host memory and y copied back and synchronised every
+step.  ``cpu_baseline`` times the CPU oracle on a bounded sample of rows.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (weak scaling; no collective on the data path).
+
+``--impl reference`` times the CPU oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "PN GEMV µs and effective HBM GB/s (% of GB300 peak) at M=1 and M=8"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+ROTATE_BYTES = 300e6           # > 2x the 129 MB L2
+GRAPH_NODES = 1000
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--algo", choices=["auto", "tc", "cuda_core"], default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers ---
+
+def workload(cfg: int):
+    from bit_weight_only_pn_gb300 import synth
+    c = synth.CONFIGS[cfg]
+    return c["name"], list(c["tensors"]), c["M"]
+
+
+def per_block(t: int) -> int:
+    return 80 if t == 124 else 64
+
+
+def algorithmic_bytes(tensors, M: int) -> int:
+    """Packed weights + fp16 x + fp32 y of one step (what the method must move)."""
+    total = 0
+    for t, K, N in tensors:
+        total += N * (K // per_block(t)) * 34 + 2 * M * K + 4 * M * N
+    return total
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("pn_gemv_tc.cu", "pn_device.cuh"):
+        with open(os.path.join(ROOT, "bit_weight_only_pn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(cfg: int):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "pn_gemv_tc_traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    want = kernel_source_hash()
+    for m in re.finditer(r"^traffic config=(\d+) bytes_per_launch=(\d+) source=([0-9a-f]+)", text, re.M):
+        if int(m.group(1)) == cfg and m.group(3) == want:
+            return int(m.group(2))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        lo, hi = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
+        sm, smax, reasons, n = [], None, set(), 0
+        for ts, line in self.lines:
+            if not (lo - 0.15 <= ts <= hi + 0.15):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            n += 1
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": n}
+
+
+# -------------------------------------------------------------- CPU oracle ---
+
+def oracle_sample_rate(tensors, M, seconds, threads):
+    """Time the CPU oracle on a bounded sample of every tensor's rows; returns
+    (GB/s of algorithmic bytes, description, threads used)."""
+    import oracle
+    from bit_weight_only_pn_gb300 import synth
+    o = oracle.Oracle()
+    # calibrate on 64 rows of the first tensor
+    t0, K0, N0 = tensors[0]
+    w = synth.weight_rows(synth.weight_seed(9, 0), N0, K0, range(64))
+    W = o.pack(t0, w)
+    x = synth.activations(synth.x_seed(9, 0), M, K0)
+    s = time.perf_counter()
+    o.gemv(t0, W, K0, x, want_abs=False)
+    per_row = (time.perf_counter() - s) / 64.0 / max(1, threads) * 1.3
+    total_rows = sum(N for _, _, N in tensors)
+    frac = min(1.0, seconds / max(per_row * total_rows, 1e-9))
+    work = []
+    for e, (t, K, N) in enumerate(tensors):
+        rows = max(16, int(N * frac))
+        rows = min(rows, N)
+        w = synth.weight_rows(synth.weight_seed(9, e), N, K, range(rows))
+        work.append((t, K, rows, o.pack(t, w), synth.activations(synth.x_seed(9, e), M, K)))
+    s = time.perf_counter()
+    for t, K, rows, W, x in work:
+        o.gemv_threads(t, W, K, x, threads)
+    dt = time.perf_counter() - s
+    nbytes = sum(rows * (K // per_block(t)) * 34 + 2 * M * K + 4 * M * rows for t, K, rows, _, _ in work)
+    desc = ", ".join(f"{rows}/{N} rows of the {K}->{N} tensor" for (t, K, rows, _, _), (_, _, N) in zip(work, tensors))
+    return nbytes / dt / 1e9, f"{desc}, M={M}, {dt:.1f} s", threads, dt
+
+
+# ------------------------------------------------------------- distributed ---
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return world, rank, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------- arms ----
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm (rank 0 only): each step runs the
+    oracle GEMV on a fixed sample of rows of every tensor, sized so that the
+    warm-up and timed steps together take about two minutes."""
+    if rank != 0:
+        return
+    import oracle
+    from bit_weight_only_pn_gb300 import synth
+    name, tensors, M = workload(args.config)
+    o = oracle.Oracle()
+    threads = os.cpu_count() or 1
+    t0, K0, N0 = tensors[0]
+    W = o.pack(t0, synth.weight_rows(synth.weight_seed(9, 0), N0, K0, range(64)))
+    x = synth.activations(synth.x_seed(9, 0), M, K0)
+    s0 = time.perf_counter()
+    o.gemv(t0, W, K0, x, want_abs=False)
+    per_row = (time.perf_counter() - s0) / 64.0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    total_rows = sum(N for _, _, N in tensors)
+    frac = min(1.0, budget / max(per_row * total_rows, 1e-12))
+    work = []
+    for e, (t, K, N) in enumerate(tensors):
+        rows = min(N, max(1, int(round(N * frac))))
+        W = o.pack(t, synth.weight_rows(synth.weight_seed(9, e), N, K, range(rows)))
+        work.append((t, K, rows, W, synth.activations(synth.x_seed(9, e), M, K)))
+    sample_rows = sum(r for _, _, r, _, _ in work)
+    use = threads if sample_rows >= 64 * threads else 1
+    nbytes = sum(r * (K // per_block(t)) * 34 + 2 * M * K + 4 * M * r for t, K, r, _, _ in work)
+
+    def one():
+        for t, K, r, W, x in work:
+            if use > 1:
+                o.gemv_threads(t, W, K, x, use)
+            else:
+                o.gemv(t, W, K, x, want_abs=False)
+
+    for _ in range(args.warmup):
+        one()
+    s0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - s0
+    value = nbytes * args.steps / dt / 1e9
+    desc = ", ".join(f"{r}/{N} rows of {'pn3t' if t == 124 else 'pn4t'} {K}->{N}"
+                     for (t, K, r, _, _), (_, _, N) in zip(work, tensors))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": name, "M": M,
+                   "oracle": "plain C, fp64 accumulation, rows split over threads"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": use, "kind": "oracle",
+                         "sample": f"each step: {desc}, M={M}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from bit_weight_only_pn_gb300 import build, pn, synth
+    if rank == 0 or not os.path.exists(pn.LIBRARY):
+        build.build()             # no-op when the library is up to date
+    dist_barrier(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name, tensors, M = workload(args.config)
+    algo = {"auto": pn.ALGO_AUTO, "tc": pn.ALGO_TENSOR_CORE, "cuda_core": pn.ALGO_CUDA_CORE}[args.algo]
+    step_bytes = algorithmic_bytes(tensors, M)
+    wbytes = sum(N * (K // per_block(t)) * 34 for t, K, N in tensors)
+    copies = max(2, int(np.ceil(ROTATE_BYTES / wbytes)))
+
+    # Inputs: seeded fp32 weights quantised on the device by pn_pack, x fp16.
+    sets = []
+    for e, (t, K, N) in enumerate(tensors):
+        w = torch.from_numpy(synth.weights(synth.weight_seed(args.config, e), N, K)).to(dev)
+        W0 = pn.pack(t, w)
+        del w
+        xs = torch.from_numpy(synth.activations(synth.x_seed(args.config, e), M, K)).to(dev)
+        sets.append((t, K, N, W0, xs))
+    rot = []
+    for c in range(copies):
+        entries = []
+        for t, K, N, W0, xs in sets:
+            W = W0 if c == 0 else W0.clone()
+            y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            entries.append((t, W, K, xs, y))
+        rot.append(entries)
+    total_rows = sum(N for _, _, N in tensors)
+    ws = pn.Workspace(total_rows, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(entries):
+        if len(entries) == 1:
+            t, W, K, x, y = entries[0]
+            pn.gemv(t, W, K, x, y=y, workspace=ws, algo=algo, stream=stream)
+        else:
+            pn.gemv_layer(entries, M, workspace=ws, algo=algo, stream=stream)
+
+    # warm up eagerly (also sets the kernel's shared-memory attribute)
+    with torch.cuda.stream(stream):
+        for i in range(min(args.warmup, 3 * copies)):
+            step(rot[i % copies])
+    torch.cuda.synchronize(dev)
+    if ws.status(stream) != 0:
+        raise RuntimeError("device-side error during warm-up")
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(rot[i % copies])
+        return g
+
+    nodes = max(1, min(GRAPH_NODES, args.steps))
+    g_full = capture(nodes)
+    rem = args.steps % nodes
+    g_rem = capture(rem) if rem else None
+    reps = args.steps // nodes
+
+    # warm-up steps through the graph
+    wrem = args.warmup
+    with torch.cuda.stream(stream):
+        while wrem >= nodes:
+            g_full.replay()
+            wrem -= nodes
+        for i in range(wrem):
+            step(rot[i % copies])
+    torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(local)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    clocks.start()
+    time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.mark()
+    start.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark()
+    dist_barrier(world)
+    clock_info = clocks.stop()
+    ms = start.elapsed_time(end)
+    ms = dist_max(world, ms)
+    status = ws.status(stream)
+    if status != 0:
+        raise RuntimeError(f"device-side error in the timed region: {status}")
+    ms_per_step = ms / args.steps
+    value = world * step_bytes * args.steps / (ms / 1e3) / 1e9
+
+    # end to end through the public API: pinned x in, pinned y out, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        xh = [torch.from_numpy(synth.activations(synth.x_seed(args.config, e) + 1000, M, K)).pin_memory()
+              for e, (t, K, N) in enumerate(tensors)]
+        yh = [torch.empty((M, N), dtype=torch.float32).pin_memory() for (t, K, N) in tensors]
+        h2d = sum(x.numel() * 2 for x in xh)
+        d2h = sum(y.numel() * 4 for y in yh)
+        n_e2e = args.e2e_steps
+
+        def e2e_step(i):
+            entries = rot[i % copies]
+            for (t, W, K, x, y), xhost in zip(entries, xh):
+                x.copy_(xhost, non_blocking=True)
+            step(entries)
+            for (t, W, K, x, y), yhost in zip(entries, yh):
+                yhost.copy_(y, non_blocking=True)
+            stream.synchronize()
+
+        with torch.cuda.stream(stream):
+            for i in range(min(20, n_e2e)):
+                e2e_step(i)
+            dist_barrier(world)
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(n_e2e):
+                e2e_step(i)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        e_ms = dist_max(world, e0.elapsed_time(e1))
+        e2e = {"value": world * step_bytes * n_e2e / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "us_per_step": e_ms * 1e3 / n_e2e, "steps": n_e2e,
+               "path": "pinned x -> device, pn_gemv via the Python binding, y -> pinned host, "
+                       "stream synchronised each step; weights resident"}
+
+    peak, peak_kind = measured_peak()
+    per_gpu = step_bytes / (ms_per_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s",
+                "frac": per_gpu / peak, "traffic": recorded_traffic(args.config),
+                "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                               if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, desc, used, _ = oracle_sample_rate(tensors, M, args.cpu_seconds, os.cpu_count() or 1)
+        cpu = {"value": rate, "unit": "GB/s", "cores": used, "kind": "oracle", "sample": desc}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 products, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": name, "M": M,
+                   "tensors": [f"{'pn3t' if t == 124 else 'pn4t'} {K}->{N}" for t, K, N in tensors],
+                   "algorithmic_bytes_per_step": step_bytes, "weight_bytes_per_step": wbytes,
+                   "l2": f"{copies} rotating weight copies ({copies * wbytes / 1e6:.0f} MB > 2x L2)",
+                   "launch": f"CUDA graph of {nodes} steps, replayed",
+                   "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "algo": args.algo},
+        "us_per_gemv": ms_per_step * 1e3,
+        "pct_of_nominal_8tbs": per_gpu / NOMINAL_HBM_GBS * 100.0,
+        "gpu_launches": args.steps * (1 if len(tensors) == 1 or algo != pn.ALGO_CUDA_CORE else len(tensors)),
+        "roofline": roofline,
+        "clocks": clock_info,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -15,6 +15,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_cc_major[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<int> g_test_stall{0};
 
 int per_block(int type) { return type == PN_TYPE_PN3T ? 80 : (type == PN_TYPE_PN4T ? 64 : 0); }
 
@@ -91,7 +92,8 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
     if (ntc > 0) {
         if (!ws || !aligned(ws, 256)) return PN_EINVAL;
         int too_small = 0;
-        cudaError_t e = pn::launch_gemv_tc(tc, ntc, M, ws, ws_bytes, sms, g_timeout_ns.load(), s, &too_small);
+        cudaError_t e = pn::launch_gemv_tc(tc, ntc, M, ws, ws_bytes, sms, g_timeout_ns.load(),
+                                           g_test_stall.load(), s, &too_small);
         if (too_small) return PN_EINVAL;
         if (e != cudaSuccess) return PN_ECUDA;
     }
@@ -224,5 +226,7 @@ pn_status pn_gemv_layer(const pn_gemv_desc* descs, int count, int M, void* works
 }
 
 void pn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
+
+void pn_set_test_stall(int on) { g_test_stall.store(on ? 1 : 0); }
 
 }  // extern "C"

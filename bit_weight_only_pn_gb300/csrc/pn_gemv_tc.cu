@@ -10,29 +10,36 @@
 //
 // Design (GB300-first; the pages' sm_60 and sm_70 kernels are prior art):
 //  * Work unit = one 16-row tile x one 8-block chunk (8 x 34 = 272 bytes per
-//    row, 16-byte aligned whenever the row is).  Units are numbered per group of
-//    8 tiles, chunk-major, tile-minor, over every tensor of the call, and the
-//    persistent grid (at most one CTA per SM) splits that sequence into equal
-//    contiguous ranges, so every SM streams the same number of bytes.
-//  * One producer warp per CTA issues cp.async.bulk copies (TMA engine, no
-//    tensor map) of each step's rows and x chunk into a 4-stage shared-memory
-//    ring, completing on mbarriers; 8 consumer warps (one per tile of the
-//    group) decode and multiply.  Every wait is bounded in time.
+//    row, 16-byte aligned whenever the row is).  Units are numbered tile-major
+//    over every tensor of the call and the persistent grid (at most one CTA per
+//    SM, each range at least one tile long) splits them into equal contiguous
+//    ranges, so every SM streams the same number of bytes and only a CTA's
+//    first and last tile can be shared, each with one neighbour.
+//  * A CTA walks its tiles in batches of up to 8 consecutive tiles of one
+//    tensor, chunk by chunk (one step = one chunk of the batch's tiles, so the
+//    activation chunk is staged once for 8 tiles), last batch first so that
+//    the shared tiles are settled early.
+//  * One producer warp issues, per step, one tiled 2-D TMA copy per tile (a
+//    tensor map over the PN rows, 16-row x 272-byte box) and one bulk copy per
+//    activation row into a 4-stage shared-memory ring completing on mbarriers.
+//    Sixteen consumer warps, two per tile, each decode four of a chunk's eight
+//    blocks.  An epilogue warp adds each tile's two halves (fixed order) and
+//    stores it, or, for a shared tile, deposits its part and lets the last of
+//    the two CTAs add both parts (fixed order), so results are deterministic.
+//    Every wait is bounded in time.
 //  * Decode: code words are read from shared memory as aligned 32-bit words
-//    (blocks at even offsets are realigned with one byte-permute per word);
-//    a LOP3 + HFMA2 per code pair turns two codes into the exact half2
-//    (n - z, n' - z), which is exactly an A-fragment register of
-//    m16n8k16 (rows g and g+8 of the tile, k pairs from code words 2t, 2t+1);
-//    x is read as B fragments straight from the staged chunk; each block's
-//    product sum starts from zero and is scaled by its d in fp32 (FFMA), so
-//    every product is exact and every sum is an fp32 sum.
-//  * Tiles split between CTAs are summed by their last contributor, in CTA
-//    order, from partial slots in the workspace (a per-tile counter decides
-//    who is last and is reset by it), so the result is deterministic.
+//    (blocks at even offsets are realigned with one byte-permute per word); a
+//    LOP3 + HFMA2 per code pair turns two codes into the exact half2
+//    (n - z, n' - z), which is exactly an A-fragment register of m16n8k16
+//    (rows g and g+8 of the tile, k pairs from code words 2t, 2t+1); x is read
+//    as B fragments straight from the staged chunk; each block's product sum
+//    starts from zero and is scaled by its d in fp32, so every product is
+//    exact and every sum is an fp32 sum.
 #include <cstdint>
 #include <type_traits>
 #include <utility>
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -42,63 +49,97 @@
 namespace pn {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kBatchTiles = 8;                          // tiles per batch (one per warp pair)
+constexpr int kTileWarps = 2;                           // warps sharing a tile, 4 blocks each
+constexpr int kConsumerWarps = kBatchTiles * kTileWarps;
+constexpr int kProducerWarp = kConsumerWarps;           // warp 16
+constexpr int kEpilogueWarp = kConsumerWarps + 1;       // warp 17
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kTileRows = 16;
-constexpr int kGroupTiles = kConsumerWarps;             // one tile per consumer warp
-constexpr int kGroupRows = kGroupTiles * kTileRows;     // 128
 constexpr int kChunkBlocks = 8;
+constexpr int kWarpBlocks = kChunkBlocks / kTileWarps;  // blocks of a chunk per warp
 constexpr int kChunkBytes = kChunkBlocks * kBlockBytes; // 272
-constexpr int kRowPitch = 288;                          // staged row pitch (bank spread)
-constexpr int kTileBytes = kTileRows * kRowPitch;
-constexpr int kStageWBytes = kGroupTiles * kTileBytes;  // 36864
+constexpr int kRowPitch = kChunkBytes;                  // rows land densely (TMA box)
+constexpr int kBoxWords = kChunkBytes / 4;              // box inner extent, 32-bit elements
+constexpr int kTileBytes = kTileRows * kRowPitch;       // 4352
+constexpr int kStageWBytes = kBatchTiles * kTileBytes;  // 34816
 constexpr int kXPitchPn3t = kChunkBlocks * 80 * 2 + 16; // 1296
 constexpr int kXPitchPn4t = kChunkBlocks * 64 * 2 + 16; // 1040
-constexpr int kStageXBytes = kMaxM * kXPitchPn3t;       // 10368
+// Activations: one block of M rows per chunk lane, each block 128-byte aligned
+// (a tiled TMA destination); lanes * M <= 8, so 8 blocks of one row of the
+// pn3t pitch rounded up to 128 bytes always fit.
+constexpr int kStageXBytes = 8 * ((kXPitchPn3t + 127) / 128 * 128);   // 11264
 constexpr int kStageBytes = kStageWBytes + kStageXBytes;
 constexpr int kStages = 4;
-constexpr int kBarrierOffset = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarrierOffset + 2 * kStages * 8 + 16;
+// Finished tile sums handed to the epilogue warp: [tile][buffer][half][lane] float4.
+constexpr int kOutBuffers = 2;
+constexpr int kOutOffset = kStages * kStageBytes;
+constexpr int kOutBytes = kBatchTiles * kOutBuffers * kTileWarps * 32 * 16;
+constexpr int kBarrierOffset = kOutOffset + kOutBytes;
+constexpr int kNumBarriers = 2 * kStages + 2 * kBatchTiles * kOutBuffers;
+constexpr int kSmemBytes = kBarrierOffset + kNumBarriers * 8 + 16;
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                  // PN_ETIMEOUT
-constexpr int kSlotFloats = kTileRows * kMaxM;          // 128
+constexpr int kSlotFloats = kTileRows * kMaxM;          // 128: one tile's partial sums
 
-static_assert(kStageWBytes % 16 == 0 && kStageBytes % 16 == 0, "TMA needs 16-byte alignment");
+static_assert(kStageWBytes % 128 == 0 && kStageBytes % 128 == 0, "TMA destinations stay aligned");
+static_assert(kMaxM * kXPitchPn3t <= kStageXBytes, "one block of 8 activation rows fits");
+
+// Bytes between the activation blocks of consecutive chunk lanes.
+__host__ __device__ constexpr int x_block_bytes(int M, int pitch) { return (M * pitch + 127) / 128 * 128; }
 
 struct TcTensor {
     const uint8_t* W;
     const uint16_t* x;
     float* y;
-    int64_t unit_base;      // first unit of this tensor in the launch's sequence
+    uint32_t unit_base;     // first unit of this tensor (tile-major, chunk-minor)
     int N;
     int nb;
     int type;
     int chunks;             // nb / 8
     int tiles;              // ceil(N / 16)
-    int group_base;         // first global group index
-    int tile_base;          // first global tile index (counter index)
 };
 
+constexpr int kBoxSizes = 4;       // row boxes of 1, 2, 4, 8 tiles
+
 struct TcParams {
+    // per tensor: PN rows as uint32 [N][row_bytes/4]; box 68 words x (16 << k) rows
+    CUtensorMap wmap[kBoxSizes][kMaxLayer];
+    // per tensor: activations as uint64 [M][K/4]; box = one chunk + 16 bytes x M rows,
+    // so consecutive rows land at the padded pitch (the extra 16 bytes are unused)
+    CUtensorMap xmap[kMaxLayer];
     TcTensor t[kMaxLayer];
     int count;
     int M;
     int grid;
-    int64_t units;
+    uint32_t units;                // units * grid < 2^32 (checked on the host)
     uint32_t* status;
-    uint32_t* counters;
-    float* partials;
+    uint32_t* counters;            // one per CTA boundary
+    float* partials;               // [boundary][side][kSlotFloats]
     uint64_t timeout_ns;
+    int stall_first_step;          // testing aid: see pn_set_test_stall
 };
 
-struct Step {
-    int e;       // tensor
-    int g;       // group within the tensor
-    int c;       // chunk
-    int jlo;     // first tile of the group in this step
-    int jhi;     // one past the last
-    int tg;      // tiles in the group
+// One batch: tiles [tb, tb + nt) of tensor e; its first tile starts at chunk
+// cs0 and its last tile ends at chunk ce_last (a CTA boundary may cut them).
+// A batch of fewer than 8 tiles gives each tile `lanes` warp pairs, which
+// take consecutive chunks: warp pair p works on tile p / lanes, chunk
+// c + p % lanes of each step.
+struct Batch {
+    int e, tb, nt, cs0, ce_last, lanes, lanes_log2, chunks;
 };
+
+
+// Whether warp pair p has work in the step of batch b starting at chunk c,
+// and which tile (batch-relative) and chunk it takes.
+__device__ __forceinline__ bool slot_work(const Batch& b, int c, int p, int& j, int& chunk) {
+    j = p >> b.lanes_log2;
+    chunk = c + (p & (b.lanes - 1));
+    if (j >= b.nt) return false;
+    const int cs = j == 0 ? b.cs0 : 0;
+    const int ce = j == b.nt - 1 ? b.ce_last : b.chunks;
+    return chunk >= cs && chunk < ce;
+}
 
 template <int N, typename Fn, int... I>
 __device__ __forceinline__ void static_for_impl(Fn&& fn, std::integer_sequence<int, I...>) {
@@ -109,45 +150,91 @@ __device__ __forceinline__ void static_for(Fn&& fn) {
     static_for_impl<N>(fn, std::make_integer_sequence<int, N>{});
 }
 
-__device__ __forceinline__ int tensor_of(const TcParams& P, int64_t u) {
-    int e = 0;
+// First unit of CTA c's range.
+__device__ __forceinline__ uint32_t range_start(const TcParams& P, int c) {
+    return P.units * static_cast<uint32_t>(c) / static_cast<uint32_t>(P.grid);
+}
+
+// Tensor, tile and chunk of unit u.
+__device__ __forceinline__ void locate(const TcParams& P, uint32_t u, int& e, int& tile, int& c) {
+    e = 0;
     while (e + 1 < P.count && u >= P.t[e + 1].unit_base) ++e;
-    return e;
+    const uint32_t rel = u - P.t[e].unit_base;
+    tile = static_cast<int>(rel / static_cast<uint32_t>(P.t[e].chunks));
+    c = static_cast<int>(rel - static_cast<uint32_t>(tile) * P.t[e].chunks);
 }
 
-__device__ __forceinline__ int group_id_of(const TcParams& P, int64_t u) {
-    const int e = tensor_of(P, u);
-    const TcTensor& T = P.t[e];
-    return T.group_base + static_cast<int>((u - T.unit_base) / (8LL * T.chunks));
-}
+// Walks a CTA's unit range [u0, u1) batch by batch.  The batches are the
+// windows of 8 tiles that start at the range's first tile (and at tile 0 of
+// each later tensor); the last one is walked first, then the others in order.
+// Within a batch the steps are c = cstart, cstart + lanes, ... < cend.
+struct Walker {
+    int e0, t0, c0, e1, t1, c1e;    // first unit; last unit's tensor, tile, chunk + 1
+    Batch cur;
+    int lastE, lastTb;              // the last batch
+    int seq;                        // batches started so far
+    int cstart, cend;               // step range of the current batch
+    bool done;
 
-// First unit of CTA c's range and the CTA whose range holds unit u.
-__device__ __forceinline__ int64_t range_start(const TcParams& P, int c) {
-    return P.units * c / P.grid;
-}
-__device__ __forceinline__ int cta_of(const TcParams& P, int64_t u) {
-    return static_cast<int>(((u + 1) * P.grid - 1) / P.units);
-}
+    __device__ Batch make(const TcParams& P, int e, int tb) const {
+        Batch b;
+        b.e = e;
+        b.tb = tb;
+        int nt = min(kBatchTiles, P.t[e].tiles - tb);
+        if (e == e1) nt = min(nt, t1 - tb + 1);
+        b.nt = nt;
+        b.cs0 = (e == e0 && tb == t0) ? c0 : 0;
+        b.ce_last = (e == e1 && tb + nt - 1 == t1) ? c1e : P.t[e].chunks;
+        // chunk lanes: a power of two, as many as the 8 warp pairs and the 8
+        // staged activation rows allow, no more than the tile has chunks
+        const int cap = min(min(kBatchTiles / nt, kMaxM / P.M), P.t[e].chunks);
+        b.lanes_log2 = cap >= 8 ? 3 : cap >= 4 ? 2 : cap >= 2 ? 1 : 0;
+        b.lanes = 1 << b.lanes_log2;
+        b.chunks = P.t[e].chunks;
+        return b;
+    }
+    __device__ void start(const Batch& b) {
+        cur = b;
+        // only a batch of one tile can start late and end early at once
+        cstart = b.nt == 1 ? b.cs0 : 0;
+        cend = b.nt == 1 ? b.ce_last : b.chunks;
+        ++seq;
+    }
+    __device__ void init(const TcParams& P, uint32_t u0, uint32_t u1) {
+        seq = -1;
+        done = u1 <= u0;
+        if (done) return;
+        locate(P, u0, e0, t0, c0);
+        int c1;
+        locate(P, u1 - 1, e1, t1, c1);
+        c1e = c1 + 1;
+        lastE = e1;
+        lastTb = (e1 == e0) ? t0 + kBatchTiles * ((t1 - t0) / kBatchTiles)
+                            : kBatchTiles * (t1 / kBatchTiles);
+        start(make(P, lastE, lastTb));
+    }
+    // Moves to the batch after `cur` in processing order; done when none is left.
+    __device__ void next_batch(const TcParams& P) {
+        int e, tb;
+        if (seq == 0) {                       // the last batch was first; now the first
+            e = e0;
+            tb = t0;
+        } else {
+            e = cur.e;
+            tb = cur.tb + kBatchTiles;
+            if (tb >= P.t[e].tiles) { ++e; tb = 0; }
+        }
+        if (e == lastE && tb == lastTb) { done = true; return; }
+        start(make(P, e, tb));
+    }
+};
 
-// Walks a CTA's unit range one step (same tensor, group and chunk) at a time.
-struct StepIter {
-    int64_t u, end;
-    __device__ bool next(const TcParams& P, Step& st) {
-        if (u >= end) return false;
-        const int e = tensor_of(P, u);
-        const TcTensor& T = P.t[e];
-        const int64_t rel = u - T.unit_base;
-        const int64_t gsz = 8LL * T.chunks;
-        const int g = static_cast<int>(rel / gsz);
-        const int tg = min(kGroupTiles, T.tiles - g * kGroupTiles);
-        const int64_t r2 = rel - g * gsz;
-        const int c = static_cast<int>(r2 / tg);
-        const int j = static_cast<int>(r2 - static_cast<int64_t>(c) * tg);
-        const int64_t left = end - u;
-        const int jhi = static_cast<int>(min(static_cast<int64_t>(tg), j + left));
-        st.e = e; st.g = g; st.c = c; st.jlo = j; st.jhi = jhi; st.tg = tg;
-        u += jhi - j;
-        return true;
+// Position in the stage ring.
+struct Ring {
+    int s = 0;
+    uint32_t phase = 0;
+    __device__ void advance() {
+        if (++s == kStages) { s = 0; phase ^= 1u; }
     }
 };
 
@@ -157,27 +244,56 @@ __device__ __forceinline__ void raise_timeout(const TcParams& P, volatile uint32
 }
 
 // Waits for phase `parity` of an mbarrier; gives up after limit_ns, or as soon
-// as another warp of the CTA has aborted (abort_flag may be null).
+// as another warp of the CTA has aborted (abort_flag may be null).  Between
+// probes the thread sleeps briefly, so waiting warps leave most issue slots
+// to the warps that are decoding.
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                              volatile uint32_t* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
+        __nanosleep(20);
         if (mbar_try_wait(bar, parity)) return true;
         if (abort_flag && *abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
+// Warp-level wait: lane 0 polls the barrier, the warp learns the outcome by
+// shuffle and __syncwarp orders the other lanes' later shared-memory reads
+// after lane 0's observation of the completed phase.  One poller per warp
+// keeps the barrier traffic 32x below every-lane polling.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                          volatile uint32_t* abort_flag, int lane) {
+    bool ok = true;
+    if (lane == 0) ok = wait_bounded(bar, parity, limit_ns, abort_flag);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();
+    return ok;
+}
+
+// Warp-level arrive: after __syncwarp (all lanes' reads of the stage are done)
+// lane 0 arrives once for the warp.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
 // ----------------------------------------------------------------- decode --
+
+// Fragment row g (and g + 8) of a tile reads staged row tile_row(g) (and +8).
+// Rows land 272 bytes (68 banks, 4 mod 32) apart; taking the even rows for
+// g = 0..3 and the odd rows for g = 4..7 makes every 64-bit load of a
+// half-warp hit 32 distinct banks.
+__device__ __forceinline__ int tile_row(int g) { return ((g & 3) << 1) | (g >> 2); }
 
 // Loads code words 2t and 2t+1 of block B of a staged row (8-byte aligned).
 template <int B>
-__device__ __forceinline__ void load_words(uint32_t row, int t, uint32_t& w0, uint32_t& w1) {
+__device__ __forceinline__ void load_words(const uint8_t* row, int t, uint32_t& w0, uint32_t& w1) {
     constexpr int kOff = B * kBlockBytes;
     if constexpr (B % 2 == 0) {
         // block starts 4-byte aligned: its words start 2 bytes into aligned words
-        const uint32_t a = row + kOff + 8 * t;
+        const uint8_t* a = row + kOff + 8 * t;
         uint32_t v0, v1, v2;
         if constexpr (kOff % 8 == 0) {
             const uint2 p = lds_u64(a);
@@ -191,7 +307,7 @@ __device__ __forceinline__ void load_words(uint32_t row, int t, uint32_t& w0, ui
         w1 = realign16(v1, v2);
     } else {
         // block starts 2 bytes past a 4-byte boundary: its words are aligned
-        const uint32_t a = row + kOff + 2 + 8 * t;
+        const uint8_t* a = row + kOff + 2 + 8 * t;
         if constexpr ((kOff + 2) % 8 == 0) {
             const uint2 p = lds_u64(a);
             w0 = p.x; w1 = p.y;
@@ -204,22 +320,16 @@ __device__ __forceinline__ void load_words(uint32_t row, int t, uint32_t& w0, ui
 
 // x pairs for code words 2t (xb[0..P-1]) and 2t+1 (xb[P..2P-1]) of block B.
 template <int TYPE, int B>
-__device__ __forceinline__ void load_x(uint32_t xrow, int t, bool on, uint32_t (&xb)[2 * Format<TYPE>::kPairs]) {
+__device__ __forceinline__ void load_x(const uint8_t* xrow, int t, uint32_t (&xb)[2 * Format<TYPE>::kPairs]) {
     using F = Format<TYPE>;
-    if (!on) {
-#pragma unroll
-        for (int i = 0; i < 2 * F::kPairs; ++i) xb[i] = 0u;
-        return;
-    }
-    if constexpr (TYPE == kPn3t) {
-        const uint32_t a = xrow + (B * F::kPerBlock + 2 * F::kPerWord * t) * 2;   // 8-byte aligned
+    const uint8_t* a = xrow + (B * F::kPerBlock + 2 * F::kPerWord * t) * 2;
+    if constexpr (TYPE == kPn3t) {                      // 8-byte aligned
 #pragma unroll
         for (int i = 0; i < 5; ++i) {
             const uint2 p = lds_u64(a + 8 * i);
             xb[2 * i] = p.x; xb[2 * i + 1] = p.y;
         }
-    } else {
-        const uint32_t a = xrow + (B * F::kPerBlock + 2 * F::kPerWord * t) * 2;   // 16-byte aligned
+    } else {                                            // 16-byte aligned
         const uint4 p = lds_u128(a);
         const uint4 q = lds_u128(a + 16);
         xb[0] = p.x; xb[1] = p.y; xb[2] = p.z; xb[3] = p.w;
@@ -227,31 +337,32 @@ __device__ __forceinline__ void load_x(uint32_t xrow, int t, bool on, uint32_t (
     }
 }
 
-// One consumer warp: the 16 rows of its tile times one 8-block chunk.  The
-// chunk's eight scaled block sums are added up first and then added to the
-// running sum, which keeps every fp32 summation chain short (at most 8 block
-// terms + one term per chunk), whatever K is.
-template <int TYPE>
-__device__ __forceinline__ void mma_tile_chunk(uint32_t tile, uint32_t xbase, int xpitch, int M,
-                                               int lane, float (&acc)[4]) {
+// One consumer warp: the 16 rows of its tile times blocks 4H .. 4H+3 of a
+// chunk (the other warp of the pair takes the other four).  The scaled block
+// sums are added up per call and then added to the running sum, which keeps
+// every fp32 summation chain short (at most 4 block terms + one term per
+// chunk) whatever K is.  xrow is this lane's activation row; lanes whose MMA
+// column is past M read token 0 (a B column only feeds its own, unused,
+// output column), so no lane takes a different path.
+template <int TYPE, int H>
+__device__ __forceinline__ void mma_tile_half(const uint8_t* tile, const uint8_t* xrow, int lane,
+                                              float (&acc)[4]) {
     using F = Format<TYPE>;
     const int g = lane >> 2, t = lane & 3;
-    const uint32_t r0 = tile + g * kRowPitch;
-    const uint32_t r1 = r0 + 8 * kRowPitch;
-    const bool xon = g < M;
-    const uint32_t xrow = xbase + g * xpitch;
+    const uint8_t* r0 = tile + tile_row(g) * kRowPitch;
+    const uint8_t* r1 = r0 + 8 * kRowPitch;
     float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    static_for<kChunkBlocks>([&](auto bc) {
-        constexpr int B = decltype(bc)::value;
-        const float d0 = half_bits_to_float(lds_u16(r0 + B * kBlockBytes));
-        const float d1 = half_bits_to_float(lds_u16(r1 + B * kBlockBytes));
+    static_for<kWarpBlocks>([&](auto bc) {
+        constexpr int B = H * kWarpBlocks + decltype(bc)::value;
+        const float d0 = lds_half_as_float(r0 + B * kBlockBytes);
+        const float d1 = lds_half_as_float(r1 + B * kBlockBytes);
         uint32_t w00, w10, w01, w11;        // w<word><row>: words 2t / 2t+1 of rows g / g+8
         load_words<B>(r0, t, w00, w10);
         load_words<B>(r1, t, w01, w11);
         const uint32_t s00 = w00 >> F::kHighShift, s10 = w10 >> F::kHighShift;
         const uint32_t s01 = w01 >> F::kHighShift, s11 = w11 >> F::kHighShift;
         uint32_t xb[2 * F::kPairs];
-        load_x<TYPE, B>(xrow, t, xon, xb);
+        load_x<TYPE, B>(xrow, t, xb);
         float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         static_for<F::kPairs>([&](auto pc) {
             constexpr int P = decltype(pc)::value;
@@ -273,9 +384,10 @@ __device__ __forceinline__ void mma_tile_chunk(uint32_t tile, uint32_t xbase, in
 
 // ------------------------------------------------------------------ flush --
 
-__device__ __forceinline__ void store_tile(const TcTensor& T, int M, int g, int j, int lane,
+// Row of a tile that fragment row g (and g + 8) reads, see tile_row.
+__device__ __forceinline__ void store_tile(const TcTensor& T, int M, int tile, int lane,
                                            const float (&v)[4]) {
-    const int row0 = g * kGroupRows + j * kTileRows + (lane >> 2);
+    const int row0 = tile * kTileRows + tile_row(lane >> 2);
     const int m0 = 2 * (lane & 3);
     const int rows[2] = {row0, row0 + 8};
 #pragma unroll
@@ -287,216 +399,449 @@ __device__ __forceinline__ void store_tile(const TcTensor& T, int M, int g, int 
     }
 }
 
-__device__ __forceinline__ float* slot_ptr(const TcParams& P, int cta, int which, int j) {
-    return P.partials + ((static_cast<int64_t>(cta) * 2 + which) * kGroupTiles + j) * kSlotFloats;
+// Partial sums of the tile shared across CTA boundary b (between CTA b-1 and
+// CTA b): side 0 holds CTA b-1's part (the tile's first chunks), side 1 CTA b's.
+__device__ __forceinline__ float* slot_ptr(const TcParams& P, int boundary, int side) {
+    return P.partials + (static_cast<int64_t>(boundary) * 2 + side) * kSlotFloats;
 }
 
-// Emits warp j's tile of group (e, g): stores it if this CTA covered all of
-// its chunks, else deposits a partial and lets the last contributor sum them.
-__device__ void flush_tile(const TcParams& P, const Step& st, int j, int lane, int64_t u0,
-                           int64_t u1, const float (&acc)[4]) {
-    const TcTensor& T = P.t[st.e];
-    const int64_t first = T.unit_base + 8LL * T.chunks * st.g + j;
-    const int64_t last = first + static_cast<int64_t>(T.chunks - 1) * st.tg;
-    if (first >= u0 && last < u1) {
-        store_tile(T, P.M, st.g, j, lane, acc);
-        return;
-    }
-    const int gid = T.group_base + st.g;
-    const int cta = blockIdx.x;
-    const int ca = cta_of(P, first), cb = cta_of(P, last);
-    const int own_which = (group_id_of(P, u0) == gid) ? 0 : 1;
-    const int r = lane >> 2, m0 = 2 * (lane & 3);
-    float* slot = slot_ptr(P, cta, own_which, j);
-    __stcg(reinterpret_cast<float2*>(slot + r * kMaxM + m0), make_float2(acc[0], acc[1]));
-    __stcg(reinterpret_cast<float2*>(slot + (r + 8) * kMaxM + m0), make_float2(acc[2], acc[3]));
-    __threadfence();
-    __syncwarp();
-    uint32_t* counter = P.counters + T.tile_base + st.g * kGroupTiles + j;
-    uint32_t old = 0;
-    if (lane == 0) old = atomicAdd(counter, 1u);
-    old = __shfl_sync(0xFFFFFFFFu, old, 0);
-    if (old != static_cast<uint32_t>(cb - ca)) return;          // someone else finishes it
-    __threadfence();
-    float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int c = ca; c <= cb; ++c) {                            // fixed order: deterministic
-        if (c == cta) {
+__device__ __forceinline__ uint32_t out_slot(uint32_t sbase, int tile, int buf, int half, int lane) {
+    return sbase + kOutOffset + (((tile * kOutBuffers + buf) * kTileWarps + half) * 32 + lane) * 16;
+}
+
+// The finished sums of warp pair p (first half + second half, in that
+// order), read from the hand-off slots in shared memory.
+__device__ __forceinline__ void tile_sum(uint32_t sbase, int j, int buf, int lane, float (&v)[4]) {
+    float a[4], b[4];
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3]) : "r"(out_slot(sbase, j, buf, 0, lane)) : "memory");
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(b[0]), "=f"(b[1]), "=f"(b[2]), "=f"(b[3]) : "r"(out_slot(sbase, j, buf, 1, lane)) : "memory");
 #pragma unroll
-            for (int i = 0; i < 4; ++i) sum[i] += acc[i];
+    for (int i = 0; i < 4; ++i) v[i] = a[i] + b[i];
+}
+
+// Emits the tiles of batch `b` from the epilogue warp.  Whole tiles are
+// stored.  A tile cut by a CTA boundary deposits this CTA's part; after one
+// fence the (at most two) boundary counters are bumped together; where this
+// CTA arrived second it loads the neighbour's part and stores left + right.
+// `bufs` holds each warp pair's hand-off buffer index in bit p.
+__device__ void flush_batch(const TcParams& P, const Batch& b, int lane, uint32_t sbase, uint32_t bufs) {
+    const TcTensor& T = P.t[b.e];
+    const int cta = blockIdx.x;
+    const int r = lane >> 2, m0 = 2 * (lane & 3);
+    const bool left_cut = b.cs0 > 0;                 // tile 0 began in CTA cta-1
+    const bool right_cut = b.ce_last < T.chunks;     // tile nt-1 ends in CTA cta+1
+    float vl[4] = {0.0f, 0.0f, 0.0f, 0.0f}, vr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < kBatchTiles; ++j) {
+        if (j >= b.nt) continue;
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int q = 0; q < b.lanes; ++q) {          // the tile's chunk lanes, in order
+            float w[4];
+            const int p = j * b.lanes + q;
+            tile_sum(sbase, p, (bufs >> p) & 1u, lane, w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] += w[i];
+        }
+        const bool lc = left_cut && j == 0, rc = right_cut && j == b.nt - 1;
+        if (lc) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vl[i] = v[i];
+        } else if (rc) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vr[i] = v[i];
         } else {
-            const int which = (group_id_of(P, range_start(P, c)) == gid) ? 0 : 1;
-            const float* s = slot_ptr(P, c, which, j);
-            const float2 a = __ldcg(reinterpret_cast<const float2*>(s + r * kMaxM + m0));
-            const float2 b = __ldcg(reinterpret_cast<const float2*>(s + (r + 8) * kMaxM + m0));
-            sum[0] += a.x; sum[1] += a.y; sum[2] += b.x; sum[3] += b.y;
+            store_tile(T, P.M, b.tb + j, lane, v);
         }
     }
-    store_tile(T, P.M, st.g, j, lane, sum);
-    if (lane == 0) atomicExch(counter, 0u);
+    if (!left_cut && !right_cut) return;
+    // deposit: our part of the left-cut tile is side 1 of boundary cta; of the
+    // right-cut tile, side 0 of boundary cta + 1
+    if (left_cut) {
+        float* s = slot_ptr(P, cta, 1);
+        __stcg(reinterpret_cast<float2*>(s + r * kMaxM + m0), make_float2(vl[0], vl[1]));
+        __stcg(reinterpret_cast<float2*>(s + (r + 8) * kMaxM + m0), make_float2(vl[2], vl[3]));
+    }
+    if (right_cut) {
+        float* s = slot_ptr(P, cta + 1, 0);
+        __stcg(reinterpret_cast<float2*>(s + r * kMaxM + m0), make_float2(vr[0], vr[1]));
+        __stcg(reinterpret_cast<float2*>(s + (r + 8) * kMaxM + m0), make_float2(vr[2], vr[3]));
+    }
+    __threadfence();
+    __syncwarp();
+    uint32_t old = 0;
+    if (lane == 0 && left_cut) old = atomicAdd(P.counters + cta, 1u);
+    if (lane == 1 && right_cut) old = atomicAdd(P.counters + cta + 1, 1u);
+    const bool l_last = left_cut && __shfl_sync(0xFFFFFFFFu, old, 0) == 1u;
+    const bool r_last = right_cut && __shfl_sync(0xFFFFFFFFu, old, 1) == 1u;
+    if (!l_last && !r_last) return;
+    __threadfence();
+    float2 la = make_float2(0.0f, 0.0f), lb = la, ra = la, rb = la;
+    if (l_last) {                                    // neighbour's part: side 0 of boundary cta
+        const float* s = slot_ptr(P, cta, 0);
+        la = __ldcg(reinterpret_cast<const float2*>(s + r * kMaxM + m0));
+        lb = __ldcg(reinterpret_cast<const float2*>(s + (r + 8) * kMaxM + m0));
+    }
+    if (r_last) {                                    // neighbour's part: side 1 of boundary cta+1
+        const float* s = slot_ptr(P, cta + 1, 1);
+        ra = __ldcg(reinterpret_cast<const float2*>(s + r * kMaxM + m0));
+        rb = __ldcg(reinterpret_cast<const float2*>(s + (r + 8) * kMaxM + m0));
+    }
+    if (l_last) {                                    // left part (cta-1) + right part (cta)
+        const float v[4] = {la.x + vl[0], la.y + vl[1], lb.x + vl[2], lb.y + vl[3]};
+        store_tile(T, P.M, b.tb, lane, v);
+        if (lane == 0) atomicExch(P.counters + cta, 0u);
+    }
+    if (r_last) {                                    // left part (cta) + right part (cta+1)
+        const float v[4] = {vr[0] + ra.x, vr[1] + ra.y, vr[2] + rb.x, vr[3] + rb.y};
+        store_tile(T, P.M, b.tb + b.nt - 1, lane, v);
+        if (lane == 0) atomicExch(P.counters + cta + 1, 0u);
+    }
 }
 
 // ----------------------------------------------------------------- kernel --
 
+struct Barriers {
+    uint32_t full0, empty0, ofull0, ofree0;
+    __device__ uint32_t full(int s) const { return full0 + 8 * s; }
+    __device__ uint32_t empty(int s) const { return empty0 + 8 * s; }
+    __device__ uint32_t out_full(int j, int b) const { return ofull0 + 8 * (j * kOutBuffers + b); }
+    __device__ uint32_t out_free(int j, int b) const { return ofree0 + 8 * (j * kOutBuffers + b); }
+};
+
+// Consumer side of a tile hand-off: the k-th finished sum of `tile` goes to
+// buffer k % 2 once the epilogue has emptied that buffer's previous use.
+__device__ bool handoff(const TcParams& P, const Barriers& B, uint32_t sbase, int tile, int half,
+                        int lane, uint32_t k, const float (&acc)[4], volatile uint32_t* abort_flag) {
+    const int buf = k & 1u;
+    const uint32_t use = k >> 1;
+    if (use > 0 && !warp_wait(B.out_free(tile, buf), (use - 1) & 1u, P.timeout_ns, abort_flag, lane)) {
+        if (lane == 0) raise_timeout(P, abort_flag);
+        return false;
+    }
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(out_slot(sbase, tile, buf, half, lane)), "f"(acc[0]), "f"(acc[1]), "f"(acc[2]),
+                    "f"(acc[3]) : "memory");
+    warp_arrive(B.out_full(tile, buf), lane);
+    return true;
+}
+
+// One consumer warp's steps of batch b: warp pair `slot` takes tile
+// slot >> lanes_log2 at chunk c + (slot & (lanes - 1)) of every step.
+template <int TYPE, int H>
+__device__ bool consume_batch(const TcParams& P, const Barriers& B, const Walker& it, const uint8_t* smem,
+                              int slot, int lane, int xtoken, Ring& ring, float (&acc)[4],
+                              volatile uint32_t* abort_flag) {
+    const Batch& b = it.cur;
+    constexpr int kPitch = TYPE == kPn3t ? kXPitchPn3t : kXPitchPn4t;
+    const int j = slot >> b.lanes_log2;
+    const int q = slot & (b.lanes - 1);
+    const bool in = j < b.nt;
+    const int cs = (j == 0 ? b.cs0 : 0) - q;             // work when cs <= c < ce
+    const int ce = (j == b.nt - 1 ? b.ce_last : b.chunks) - q;
+    const int toff = slot * kTileBytes;
+    const int xoff = kStageWBytes + q * x_block_bytes(P.M, kPitch) + xtoken * kPitch;
+    for (int c = it.cstart; c < it.cend; c += b.lanes) {
+        if (!warp_wait(B.full(ring.s), ring.phase, P.timeout_ns, abort_flag, lane)) {
+            if (lane == 0) raise_timeout(P, abort_flag);
+            return false;
+        }
+        if (in && c >= cs && c < ce) {
+            const uint8_t* stage = smem + ring.s * kStageBytes;
+            mma_tile_half<TYPE, H>(stage + toff, stage + xoff, lane, acc);
+        }
+        warp_arrive(B.empty(ring.s), lane);
+        ring.advance();
+    }
+    return !*abort_flag;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t full0 = sbase + kBarrierOffset;
-    const uint32_t empty0 = full0 + kStages * 8;
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kBarrierOffset + 2 * kStages * 8);
+    Barriers B;
+    B.full0 = sbase + kBarrierOffset;
+    B.empty0 = B.full0 + kStages * 8;
+    B.ofull0 = B.empty0 + kStages * 8;
+    B.ofree0 = B.ofull0 + kBatchTiles * kOutBuffers * 8;
+    volatile uint32_t* abort_flag =
+        reinterpret_cast<volatile uint32_t*>(smem + kBarrierOffset + kNumBarriers * 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kConsumerWarps);
+            mbar_init(B.full(s), 1);
+            mbar_init(B.empty(s), kConsumerWarps);
         }
+        for (int j = 0; j < kBatchTiles; ++j)
+            for (int b = 0; b < kOutBuffers; ++b) {
+                mbar_init(B.out_full(j, b), kTileWarps);
+                mbar_init(B.out_free(j, b), 1);
+            }
         *abort_flag = 0u;
         fence_mbar_init();
     }
     __syncthreads();
 
-    const int64_t u0 = range_start(P, blockIdx.x);
-    const int64_t u1 = range_start(P, blockIdx.x + 1);
+    const uint32_t u0 = range_start(P, blockIdx.x);
+    const uint32_t u1 = range_start(P, blockIdx.x + 1);
 
-    uint32_t issued[kStages];             // producer: copies issued per stage
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) issued[s] = 0;
-
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------- producer --
-        StepIter it{u0, u1};
-        Step st;
+        // Per step: one barrier wait, one expect_tx, one copy per lane.  Every
+        // per-batch quantity is computed when the batch starts, so the loop
+        // that feeds the ring stays short (this warp shares its scheduler
+        // with four decoding warps).
+        if (lane < P.count) {
+#pragma unroll
+            for (int k = 0; k < kBoxSizes; ++k) prefetch_tensormap(&P.wmap[k][lane]);
+            prefetch_tensormap(&P.xmap[lane]);
+        }
+        Walker it;
+        it.init(P, u0, u1);
+        Ring ring;
         int idx = 0;
-        while (!*abort_flag && it.next(P, st)) {
-            const int s = idx % kStages;
-            const uint32_t round = static_cast<uint32_t>(idx / kStages);
-            if (round > 0 && !wait_bounded(empty0 + 8 * s, (round - 1) & 1u, P.timeout_ns, abort_flag)) {
-                raise_timeout(P, abort_flag);
-                break;
-            }
-            const TcTensor& T = P.t[st.e];
-            const int per_blk = per_block(T.type);
-            const int xbytes = kChunkBlocks * per_blk * 2;
-            const int xpitch = T.type == kPn3t ? kXPitchPn3t : kXPitchPn4t;
-            const int row0 = st.g * kGroupRows + st.jlo * kTileRows;
-            const int rows = min((st.jhi - st.jlo) * kTileRows, T.N - row0);
-            const int64_t K = static_cast<int64_t>(T.nb) * per_blk;
-            const int64_t rb = static_cast<int64_t>(T.nb) * kBlockBytes;
-            const uint32_t full = full0 + 8 * s;
-            const uint32_t stage = sbase + s * kStageBytes;
-            if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(P.M * xbytes + rows * kChunkBytes));
-            __syncwarp();
-            const int total = P.M + rows;
-            for (int i = lane; i < total; i += 32) {
-                if (i < P.M) {
-                    bulk_g2s(stage + kStageWBytes + i * xpitch,
-                             T.x + i * K + static_cast<int64_t>(st.c) * kChunkBlocks * per_blk, xbytes, full);
+        bool stop = false;
+        while (!it.done && !stop) {
+            const Batch b = it.cur;
+            const bool p3 = P.t[b.e].type == kPn3t;
+            const int xwords = p3 ? kChunkBlocks * 80 / 4 : kChunkBlocks * 64 / 4;   // u64 per chunk
+            const int xrow_bytes = p3 ? kXPitchPn3t : kXPitchPn4t;
+            const int xblock = x_block_bytes(P.M, xrow_bytes);
+            const uint32_t xtx = static_cast<uint32_t>(P.M * xrow_bytes);
+            const void* xmap = &P.xmap[b.e];
+            const int row0 = b.tb * kTileRows;
+            for (int c = it.cstart; c < it.cend; c += b.lanes) {
+                if (*abort_flag) { stop = true; break; }
+                if (idx >= kStages && !warp_wait(B.empty(ring.s), ring.phase ^ 1u, P.timeout_ns, abort_flag, lane)) {
+                    if (lane == 0) raise_timeout(P, abort_flag);
+                    stop = true;
+                    break;
+                }
+                const int nq = min(b.lanes, b.chunks - c);
+                // tiles with a box this step
+                int jlo = 0, jhi = 0, nbox;
+                uint32_t mask = 0;
+                if (b.lanes == 1) {
+                    jlo = c < b.cs0 ? 1 : 0;
+                    jhi = c >= b.ce_last ? b.nt - 1 : b.nt;
+                    nbox = jhi - jlo;
                 } else {
-                    const int rr = i - P.M;
-                    bulk_g2s(stage + (st.jlo * kTileRows + rr) * kRowPitch,
-                             T.W + (row0 + rr) * rb + static_cast<int64_t>(st.c) * kChunkBytes,
-                             kChunkBytes, full);
+#pragma unroll
+                    for (int p = 0; p < kBatchTiles; ++p) {
+                        int j, ch;
+                        if (slot_work(b, c, p, j, ch)) mask |= 1u << p;
+                    }
+                    nbox = __popc(mask);
+                }
+                const uint32_t full = B.full(ring.s);
+                const uint32_t stage = sbase + ring.s * kStageBytes;
+                // a box past the last row or the end of x is zero-filled and still counts in full
+                if (lane == 0) mbar_arrive_expect_tx(full, nq * xtx + static_cast<uint32_t>(nbox * kTileBytes));
+                __syncwarp();
+                if (!(P.stall_first_step && idx == 0)) {
+                    if (lane < nq) {                // activation chunk c + lane, all M rows
+                        tma_load_2d(stage + kStageWBytes + lane * xblock, xmap, (c + lane) * xwords, 0, full);
+                    } else if (lane >= 8 && lane < 8 + kBatchTiles) {
+                        const int i = lane - 8;
+                        if (b.lanes == 1) {
+                            // tiles [jlo, jhi) as boxes of 8, 4, 2, 1 tiles, largest
+                            // first; this lane issues box number i
+                            int j = jlo, k = 0;
+                            for (int n = 0; j < jhi; ++n) {
+                                const int left = jhi - j;
+                                const int lg = left >= 8 ? 3 : left >= 4 ? 2 : left >= 2 ? 1 : 0;
+                                if (n == i) { k = lg; break; }
+                                j += 1 << lg;
+                            }
+                            if (j < jhi)
+                                tma_load_2d(stage + j * kTileBytes, &P.wmap[k][b.e], c * kBoxWords,
+                                            row0 + j * kTileRows, full);
+                        } else if ((mask >> i) & 1u) {
+                            tma_load_2d(stage + i * kTileBytes, &P.wmap[0][b.e],
+                                        (c + (i & (b.lanes - 1))) * kBoxWords,
+                                        row0 + (i >> b.lanes_log2) * kTileRows, full);
+                        }
+                    }
+                }
+                // (testing aid: with stall_first_step the first step's bytes
+                // are announced but never copied; its wait can only time out)
+                ring.advance();
+                ++idx;
+            }
+            if (!stop) it.next_batch(P);
+        }
+        // Every copy this warp started must land before the CTA can exit.
+        // Stage s was last filled by step s + kStages * r for the largest such
+        // step below idx; after a normal run that phase has completed (the
+        // consumers waited for it) and this returns at once; after an abort it
+        // waits, bounded, for the copies still in flight.
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+                if (idx <= s) continue;
+                const uint32_t last_round = static_cast<uint32_t>((idx - 1 - s) / kStages);
+                if (P.stall_first_step && s == 0 && last_round == 0) continue;   // never copied
+                wait_bounded(B.full(s), last_round & 1u, kDrainLimitNs, nullptr);
+            }
+        }
+    } else if (warp == kEpilogueWarp) {
+        // ------------------------------------------------------- epilogue --
+        // Walks the same batches; when a batch's warp pairs have handed off
+        // their sums it emits the batch.
+        Walker it;
+        it.init(P, u0, u1);
+        uint32_t kcount[kBatchTiles];
+#pragma unroll
+        for (int p = 0; p < kBatchTiles; ++p) kcount[p] = 0;
+        while (!it.done) {
+            const Batch& cur = it.cur;
+            const int slots = cur.nt * cur.lanes;
+            uint32_t bufs = 0;
+            bool ok = true;
+#pragma unroll
+            for (int p = 0; p < kBatchTiles; ++p) {
+                if (p >= slots || !ok) continue;
+                const int buf = kcount[p] & 1u;
+                bufs |= static_cast<uint32_t>(buf) << p;
+                if (!warp_wait(B.out_full(p, buf), (kcount[p] >> 1) & 1u, P.timeout_ns, abort_flag, lane)) {
+                    if (lane == 0) raise_timeout(P, abort_flag);
+                    ok = false;
                 }
             }
-            issued[s] = round + 1;
-            ++idx;
+            if (!ok) break;
+            flush_batch(P, cur, lane, sbase, bufs);
+#pragma unroll
+            for (int p = 0; p < kBatchTiles; ++p) {
+                if (p >= slots) continue;
+                warp_arrive(B.out_free(p, (bufs >> p) & 1u), lane);
+                ++kcount[p];
+            }
+            if (*abort_flag) break;
+            it.next_batch(P);
         }
     } else {
         // ------------------------------------------------------- consumers --
-        StepIter it{u0, u1};
-        Step st, cur{};
-        int cur_gid = -1;
-        bool active = false;
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        int idx = 0;
-        bool ok = true;
-        while (it.next(P, st)) {
-            const TcTensor& T = P.t[st.e];
-            const int gid = T.group_base + st.g;
-            if (gid != cur_gid) {
-                if (active) flush_tile(P, cur, warp, lane, u0, u1, acc);
-                active = false;
-                acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-                cur_gid = gid;
-                cur = st;
-            }
-            const int s = idx % kStages;
-            const uint32_t parity = static_cast<uint32_t>(idx / kStages) & 1u;
-            const bool got = wait_bounded(full0 + 8 * s, parity, P.timeout_ns, abort_flag);
-            if (!__all_sync(0xFFFFFFFFu, got)) {
-                if (lane == 0) raise_timeout(P, abort_flag);
-                ok = false;
+        const int slot = warp >> 1, half = warp & 1;
+        const int xtoken = (lane >> 2) < P.M ? (lane >> 2) : 0;
+        Walker it;
+        it.init(P, u0, u1);
+        Ring ring;
+        uint32_t handoffs = 0;
+        while (!it.done) {
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            bool ok;
+            if (P.t[it.cur.e].type == kPn3t)
+                ok = half == 0 ? consume_batch<kPn3t, 0>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag)
+                               : consume_batch<kPn3t, 1>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag);
+            else
+                ok = half == 0 ? consume_batch<kPn4t, 0>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag)
+                               : consume_batch<kPn4t, 1>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag);
+            if (!ok) break;
+            if (slot < it.cur.nt * it.cur.lanes &&
+                !handoff(P, B, sbase, slot, half, lane, handoffs++, acc, abort_flag))
                 break;
-            }
-            if (st.jlo <= warp && warp < st.jhi) {
-                const uint32_t stage = sbase + s * kStageBytes;
-                const uint32_t tile = stage + warp * kTileBytes;
-                const uint32_t xbase = stage + kStageWBytes;
-                if (T.type == kPn3t) mma_tile_chunk<kPn3t>(tile, xbase, kXPitchPn3t, P.M, lane, acc);
-                else mma_tile_chunk<kPn4t>(tile, xbase, kXPitchPn4t, P.M, lane, acc);
-                active = true;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
-            ++idx;
-            if (*abort_flag) { ok = false; break; }
+            it.next_batch(P);
         }
-        if (ok && active) flush_tile(P, cur, warp, lane, u0, u1, acc);
     }
-    __syncthreads();
-    // Every copy the producer started must land before the CTA exits.  After a
-    // normal run each stage's last phase has completed and this returns at
-    // once; after an abort it waits (bounded) for the copies still in flight.
-    if (warp == kConsumerWarps) {
-#pragma unroll
-        for (int s = 0; s < kStages; ++s)
-            if (issued[s]) wait_bounded(full0 + 8 * s, (issued[s] - 1) & 1u, kDrainLimitNs, nullptr);
-    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Tensor map over a tensor's PN rows viewed as uint32 [N][row_bytes / 4],
+// box = one 8-block chunk (68 words) x `rows` rows.
+bool encode_rows(CUtensorMap* map, const GemvTensor& t, int rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(t.nb) * kBlockBytes;
+    const cuuint64_t dims[2] = {row_bytes / 4, static_cast<cuuint64_t>(t.N)};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxWords), static_cast<cuuint32_t>(rows)};
+    const cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(t.W), dims, strides, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map over a tensor's activations viewed as uint64 [M][K / 4]; box =
+// one chunk plus 16 bytes (162 / 130 elements for pn3t / pn4t) x M rows.  A
+// box reaching past the end of x is zero-filled.
+bool encode_x(CUtensorMap* map, const GemvTensor& t, int M) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const int per_blk = t.type == kPn3t ? 80 : 64;
+    const cuuint64_t K = static_cast<cuuint64_t>(t.nb) * per_blk;
+    const cuuint64_t dims[2] = {K / 4, static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {K * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>((t.type == kPn3t ? kXPitchPn3t : kXPitchPn4t) / 8),
+                               static_cast<cuuint32_t>(M)};
+    const cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint16_t*>(t.x), dims, strides, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
-// The counter array starts at an offset that depends only on the device (its
-// SM count), so counters left at zero by one call are where the next call,
-// of any shape, looks for them; partial slots never overlap counters.
-WorkspaceLayout workspace_layout(int64_t total_tiles, int max_ctas) {
+// Workspace: status word, then for every CTA boundary (one more than the
+// largest grid) a counter and two partial-sum slots.
+WorkspaceLayout workspace_layout(int64_t /*total_tiles*/, int max_ctas) {
     WorkspaceLayout L;
     L.status = 0;
     L.partials = 256;
-    L.counters = L.partials + static_cast<size_t>(max_ctas) * 2 * kGroupTiles * kSlotFloats * sizeof(float);
-    L.total = L.counters + ((static_cast<size_t>(total_tiles) * 4 + 255) / 256) * 256;
+    const size_t boundaries = static_cast<size_t>(max_ctas) + 1;
+    L.counters = L.partials + boundaries * 2 * kSlotFloats * sizeof(float);
+    L.total = L.counters + ((boundaries * 4 + 255) / 256) * 256;
     return L;
 }
 
 int tc_max_ctas(int num_sms) { return num_sms; }
 
 cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, void* workspace,
-                           size_t workspace_bytes, int num_sms, uint64_t timeout_ns,
+                           size_t workspace_bytes, int num_sms, uint64_t timeout_ns, int stall,
                            cudaStream_t s, int* needs_bytes_out) {
     TcParams P{};
-    int64_t units = 0;
-    int groups = 0, tiles = 0;
+    uint64_t units = 0;
+    int max_chunks = 1;
     for (int e = 0; e < count; ++e) {
         TcTensor& T = P.t[e];
         T.W = t[e].W; T.x = t[e].x; T.y = t[e].y;
         T.N = t[e].N; T.nb = t[e].nb; T.type = t[e].type;
         T.chunks = t[e].nb / kChunkBlocks;
         T.tiles = (t[e].N + kTileRows - 1) / kTileRows;
-        T.unit_base = units;
-        T.group_base = groups;
-        T.tile_base = tiles;
-        units += static_cast<int64_t>(T.chunks) * T.tiles;
-        groups += (T.tiles + kGroupTiles - 1) / kGroupTiles;
-        tiles += T.tiles;
+        T.unit_base = static_cast<uint32_t>(units);
+        for (int k = 0; k < kBoxSizes; ++k)
+            if (!encode_rows(&P.wmap[k][e], t[e], kTileRows << k)) return cudaErrorInvalidValue;
+        if (!encode_x(&P.xmap[e], t[e], M)) return cudaErrorInvalidValue;
+        units += static_cast<uint64_t>(T.chunks) * T.tiles;
+        max_chunks = T.chunks > max_chunks ? T.chunks : max_chunks;
     }
     P.count = count;
     P.M = M;
-    P.units = units;
-    int64_t grid = units / 8;
-    if (grid > num_sms) grid = num_sms;
+    // every range spans at least one whole tile, so a tile has at most two owners
+    uint64_t grid = units / static_cast<uint64_t>(max_chunks);
+    if (grid > static_cast<uint64_t>(num_sms)) grid = num_sms;
     if (grid < 1) grid = 1;
+    if (units * grid >= (1ull << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
     P.grid = static_cast<int>(grid);
-    const WorkspaceLayout L = workspace_layout(tiles, tc_max_ctas(num_sms));
+    P.units = static_cast<uint32_t>(units);
+    const WorkspaceLayout L = workspace_layout(0, tc_max_ctas(num_sms));
     if (needs_bytes_out) *needs_bytes_out = 0;
     if (L.total > workspace_bytes) {
         if (needs_bytes_out) *needs_bytes_out = 1;
@@ -507,6 +852,7 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, void* workspac
     P.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
     P.partials = reinterpret_cast<float*>(ws + L.partials);
     P.timeout_ns = timeout_ns;
+    P.stall_first_step = stall;
 
     static bool attr_set = false;   // per process; the attribute is per function
     if (!attr_set) {

@@ -37,7 +37,7 @@ WorkspaceLayout workspace_layout(int64_t total_tiles, int max_ctas);
 // Tensor-core GEMV over `count` tensors (every one with nb % 8 == 0 and W, x
 // 16-byte aligned).  `workspace` has the layout above, zeroed.
 cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, void* workspace,
-                           size_t workspace_bytes, int num_sms, uint64_t timeout_ns,
+                           size_t workspace_bytes, int num_sms, uint64_t timeout_ns, int stall,
                            cudaStream_t s, int* needs_bytes_out);
 
 int tc_max_ctas(int num_sms);

@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
             L.pn_gemv_layer_ex.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, i32, vp]
             L.pn_set_wait_timeout_ns.restype = None
             L.pn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+            L.pn_set_test_stall.restype = None
+            L.pn_set_test_stall.argtypes = [ctypes.c_int]
             _lib = L
         return _lib
 
@@ -196,3 +198,7 @@ def gemv_layer(entries, M: int, workspace: Workspace | None = None, algo: int = 
 
 def set_wait_timeout_ns(ns: int) -> None:
     lib().pn_set_wait_timeout_ns(int(ns))
+
+
+def set_test_stall(on: bool) -> None:
+    lib().pn_set_test_stall(1 if on else 0)

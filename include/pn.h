@@ -175,6 +175,15 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
  */
 void pn_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * Testing aid for the failure path: while on (non-zero), every thread block of
+ * the tensor-core kernel announces the bytes of its first step but never
+ * copies them, so its consumers' wait can only end by timing out; the call
+ * then reports PN_ETIMEOUT through pn_workspace_status and its outputs are
+ * undefined.  Off by default.  Process-wide; not for concurrent use.
+ */
+void pn_set_test_stall(int on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -184,17 +184,21 @@ def test_workspace_too_small(pn, dev, oracle):
 
 
 def test_wait_timeout_reports_status(pn, dev, oracle):
-    # A zero time limit makes the first wait give up: the kernel must stop,
-    # let its copies land, report PN_ETIMEOUT, and leave the context usable.
+    # Each thread block announces its first step's bytes but never copies them
+    # (a barrier phase nothing completes): the waits must give up after the
+    # time limit, the kernel must let its other copies land and return, report
+    # PN_ETIMEOUT, and leave the context usable for the next call.
     N, K = 4096, 64 * 80
     W, x = synth_case(oracle, PN3T, N, K, 1, 0x99)
     Wd, xd = to_dev(W, dev), to_dev(x, dev)
     ws = pn.Workspace(N, dev)
     try:
-        pn.set_wait_timeout_ns(0)
+        pn.set_wait_timeout_ns(2_000_000)
+        pn.set_test_stall(True)
         pn.gemv(PN3T, Wd, K, xd, workspace=ws, algo=pn.ALGO_TENSOR_CORE)
         assert ws.status() == 5
     finally:
+        pn.set_test_stall(False)
         pn.set_wait_timeout_ns(1_000_000_000)
     y = pn.gemv(PN3T, Wd, K, xd, workspace=ws, algo=pn.ALGO_TENSOR_CORE).cpu().numpy()
     assert ws.status() == 0
