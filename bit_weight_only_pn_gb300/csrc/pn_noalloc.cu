@@ -1,0 +1,89 @@
+// pn_noalloc.cu -- pn_gemv_noalloc: the GEMV for callers that cannot allocate
+// device memory.
+//
+// pn_gemv needs a small device workspace (a status word, one counter per
+// thread-block boundary and two partial-sum slots per boundary) that the
+// caller allocates.  Some callers cannot allocate: code running inside a host
+// callback or a driver-managed stream where cudaMalloc is not allowed, plugins
+// whose host framework owns every allocation, or code that must never touch
+// the allocator once a model is loaded.  pn_gemv_noalloc gives them the same
+// GEMV with the workspace taken from a fixed array in this library's device
+// image instead.
+//
+// The array is a file-scope __device__ variable: every GPU that loads the
+// library holds it (kNoAllocScratchBytes) until the process exits.  In host
+// code its name is only a host-side stand-in, not a device address, so the
+// device address is looked up with cudaGetSymbolAddress once per device, with
+// that device current, and passed to the kernel like any other workspace.
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pn.h"
+#include "pn_internal.h"
+
+namespace {
+
+// Room for the workspace of a device with up to 253 SMs: the workspace size
+// depends only on the SM count s, 256 + 1024 * (s + 1) bytes plus the
+// (s + 1) counters rounded up to 256 bytes.
+constexpr size_t kNoAllocScratchBytes = 256 * 1024;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};                 // device address per device, once looked up
+
+// The scratch array's device address on the current device (looked up once).
+pn_status scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return PN_ECUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return PN_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return PN_ECUDA;
+        }
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return PN_OK;
+}
+
+}  // namespace
+
+extern "C" pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const uint16_t* x,
+                                     int M, float* y, pn_stream stream) {
+    // The workspace this call needs on the current device; beyond the fixed
+    // array (a device with more SMs than it was sized for) the call is refused.
+    const size_t need = pn_workspace_bytes(N > 0 ? N : 1);
+    if (need == 0) return PN_ECUDA;
+    if (need > kNoAllocScratchBytes) return PN_EINVAL;
+    void* ws = nullptr;
+    pn_status st = scratch_address(&ws);
+    if (st != PN_OK) return st;
+    // The array keeps the last call's contents.  The status word and the
+    // boundary counters must start at zero; a completed call leaves them zero,
+    // an aborted one may not, so both are cleared before every launch.
+    int sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PN_ECUDA;
+    }
+    const pn::WorkspaceLayout L = pn::workspace_layout(0, pn::tc_max_ctas(sms));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char* base = static_cast<unsigned char*>(ws);
+    if (cudaMemsetAsync(base + L.status, 0, L.partials - L.status, s) != cudaSuccess ||
+        cudaMemsetAsync(base + L.counters, 0, L.total - L.counters, s) != cudaSuccess) {
+        cudaGetLastError();
+        return PN_ECUDA;
+    }
+    return pn_gemv_ex(type, W, N, K, x, M, y, ws, kNoAllocScratchBytes, PN_ALGO_AUTO, stream);
+}

@@ -168,6 +168,32 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
                            size_t workspace_bytes, int algo, pn_stream stream);
 
 /*
+ * pn_gemv_noalloc: pn_gemv for callers that cannot allocate device memory --
+ * code running where cudaMalloc is not allowed (a host callback, a stream
+ * owned by another runtime), a plugin whose host framework owns every
+ * allocation, or a serving loop that must not touch the allocator once the
+ * model is loaded.  (The pages have no counterpart: this entry point only
+ * changes where the scratch memory comes from.)  Same arguments, layouts,
+ * results and alignment rules as pn_gemv; no workspace argument.
+ *
+ * Scratch: a fixed 256 KiB array in the library's device image, which every
+ * GPU that loads the library holds until the process exits.  A device whose
+ * workspace (pn_workspace_bytes) would not fit (more than 253 SMs) gets
+ * PN_EINVAL and nothing is launched.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress, which may load the
+ * library's device module); make that first call before capturing a stream
+ * into a CUDA graph.  Every call shares the array and it keeps the last call's
+ * contents: each call first clears, on `stream`, the parts that must start at
+ * zero.  Calls whose executions overlap on the GPU (other streams, other host
+ * threads) race on the array and give wrong results; order them on one
+ * stream.  A device-side wait that gives up (see pn_set_wait_timeout_ns)
+ * leaves the outputs undefined and, unlike pn_gemv, cannot be read back.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M,
+                          float* y, pn_stream stream);
+
+/*
  * Testing aid: the time limit, in nanoseconds, of every device-side wait in
  * the tensor-core kernel (default 1e9).  A wait that runs out stops its thread
  * block, which records PN_ETIMEOUT in the workspace status word and returns
