@@ -92,8 +92,13 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
     if (ntc > 0) {
         if (!ws || !aligned(ws, 256)) return PN_EINVAL;
         int too_small = 0;
-        cudaError_t e = pn::launch_gemv_tc(tc, ntc, M, ws, ws_bytes, sms, g_timeout_ns.load(),
-                                           g_test_stall.load(), s, &too_small);
+        // one or two tokens: every warp streams its own units; more: thread
+        // blocks share each staged activation chunk among eight tiles
+        cudaError_t e = M <= 2
+            ? pn::launch_gemv_warp(tc, ntc, M, ws, ws_bytes, sms, g_timeout_ns.load(), g_test_stall.load(), s,
+                                   &too_small)
+            : pn::launch_gemv_tc(tc, ntc, M, ws, ws_bytes, sms, g_timeout_ns.load(), g_test_stall.load(), s,
+                                 &too_small);
         if (too_small) return PN_EINVAL;
         if (e != cudaSuccess) return PN_ECUDA;
     }

@@ -11,6 +11,9 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
+#include <utility>
+
 #include <cuda_fp16.h>
 
 namespace pn {
@@ -107,13 +110,41 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
         :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
-// Shared-memory loads as plain C++ loads through a pointer into the kernel's
-// dynamic shared memory: the compiler may schedule them freely, but never
-// across the mbarrier waits and arrives, which are asm with memory clobbers.
+// Prefetch of one box of `tmap` from global memory into L2 (no shared-memory
+// destination, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(tmap), "r"(x), "r"(y) : "memory");
+}
+
+// Prefetch of the L1 line holding `p` (global memory).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" :: "l"(p));
+}
+
 // Brings a tensor map (a kernel parameter) into the TMA descriptor cache.
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// its later async-proxy (TMA) accesses to shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Programmatic dependent launch: let the next kernel on the stream launch
+// now / wait until the previous kernel has completed and its writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Shared-memory loads as plain C++ loads through a pointer into the kernel's
+// dynamic shared memory: the compiler may schedule them freely, but never
+// across the mbarrier waits and arrives, which are asm with memory clobbers.
 
 __device__ __forceinline__ uint32_t lds_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint2 lds_u64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
@@ -181,6 +212,98 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t word, uint32_t shifted)
         : (kOff == 0 ? 0xE408u : 0xD480u);                         // -1032, -72
     constexpr uint32_t kBias2 = kBias | (kBias << 16);
     return hfma2(and_or(kHigh ? shifted : word, kMask2, 0x64006400u), kScale2, kBias2);
+}
+
+// ------------------------------------------------- one block of a 16-row tile --
+//
+// A staged tile holds 16 rows of one 8-block chunk, 272 bytes apart.  Lane
+// (g, t) of a warp (g = lane / 4, t = lane % 4) owns MMA rows g and g + 8 and
+// code words 2t, 2t + 1 of every block; code pair P of word 2t gives the A
+// register for k = 2t, 2t + 1 and the same pair of word 2t + 1 the one for
+// k = 2t + 8, 2t + 9 of the block's P-th m16n8k16 product, so a block is
+// kPairs products whose 16 k-slots all lie in the block (one scale each).
+
+constexpr int kStagedRowBytes = 8 * kBlockBytes;    // 272: rows of a staged tile
+
+template <int N, typename Fn, int... I>
+__device__ __forceinline__ void static_for_impl(Fn&& fn, std::integer_sequence<int, I...>) {
+    (fn(std::integral_constant<int, I>{}), ...);
+}
+template <int N, typename Fn>
+__device__ __forceinline__ void static_for(Fn&& fn) {
+    static_for_impl<N>(fn, std::make_integer_sequence<int, N>{});
+}
+
+// Fragment row g (and g + 8) of a tile reads staged row tile_row(g) (and +8).
+// Rows are 272 bytes (68 banks, 4 mod 32) apart; taking the even rows for
+// g = 0..3 and the odd rows for g = 4..7 makes every 64-bit load of a
+// half-warp hit 32 distinct banks.
+__device__ __forceinline__ int tile_row(int g) { return ((g & 3) << 1) | (g >> 2); }
+
+// Loads code words 2t and 2t+1 of block B of a staged row (8-byte aligned).
+template <int B>
+__device__ __forceinline__ void load_words(const uint8_t* row, int t, uint32_t& w0, uint32_t& w1) {
+    constexpr int kOff = B * kBlockBytes;
+    if constexpr (B % 2 == 0) {
+        // block starts 4-byte aligned: its words start 2 bytes into aligned words
+        const uint8_t* a = row + kOff + 8 * t;
+        uint32_t v0, v1, v2;
+        if constexpr (kOff % 8 == 0) {
+            const uint2 p = lds_u64(a);
+            v0 = p.x; v1 = p.y; v2 = lds_u32(a + 8);
+        } else {
+            v0 = lds_u32(a);
+            const uint2 p = lds_u64(a + 4);
+            v1 = p.x; v2 = p.y;
+        }
+        w0 = realign16(v0, v1);
+        w1 = realign16(v1, v2);
+    } else {
+        // block starts 2 bytes past a 4-byte boundary: its words are aligned
+        const uint8_t* a = row + kOff + 2 + 8 * t;
+        if constexpr ((kOff + 2) % 8 == 0) {
+            const uint2 p = lds_u64(a);
+            w0 = p.x; w1 = p.y;
+        } else {
+            w0 = lds_u32(a);
+            w1 = lds_u32(a + 4);
+        }
+    }
+}
+
+// Block B of staged rows r0 (MMA row g) and r1 (row g + 8) times the x pairs
+// xb (xb[P]: word 2t, pair P; xb[kPairs + P]: word 2t + 1, pair P).  The
+// block's products start from zero and are scaled by the rows' d in fp32:
+// part[0..1] += d(r0) * (columns 2t, 2t+1), part[2..3] += d(r1) * (same).
+// With kOddCols false the odd columns (part[1], part[3]) are left alone, for
+// callers that only read even columns (a single token).
+template <int TYPE, int B, bool kOddCols = true>
+__device__ __forceinline__ void block_mma(const uint8_t* r0, const uint8_t* r1, int t,
+                                          const uint32_t (&xb)[2 * Format<TYPE>::kPairs], float (&part)[4]) {
+    using F = Format<TYPE>;
+    const float d0 = lds_half_as_float(r0 + B * kBlockBytes);
+    const float d1 = lds_half_as_float(r1 + B * kBlockBytes);
+    uint32_t w00, w10, w01, w11;        // w<word><row>: words 2t / 2t+1 of rows g / g+8
+    load_words<B>(r0, t, w00, w10);
+    load_words<B>(r1, t, w01, w11);
+    const uint32_t s00 = w00 >> F::kHighShift, s10 = w10 >> F::kHighShift;
+    const uint32_t s01 = w01 >> F::kHighShift, s11 = w11 >> F::kHighShift;
+    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    static_for<F::kPairs>([&](auto pc) {
+        constexpr int P = decltype(pc)::value;
+        const uint32_t a[4] = {
+            decode_pair<TYPE, P>(w00, s00),   // row g,   k = 2t, 2t+1   <- word 2t
+            decode_pair<TYPE, P>(w01, s01),   // row g+8, k = 2t, 2t+1   <- word 2t
+            decode_pair<TYPE, P>(w10, s10),   // row g,   k = 2t+8, 2t+9 <- word 2t+1
+            decode_pair<TYPE, P>(w11, s11)};  // row g+8, k = 2t+8, 2t+9 <- word 2t+1
+        mma_16816(c, a, xb[P], xb[F::kPairs + P], c);
+    });
+    part[0] = fmaf(d0, c[0], part[0]);
+    part[2] = fmaf(d1, c[2], part[2]);
+    if constexpr (kOddCols) {
+        part[1] = fmaf(d0, c[1], part[1]);
+        part[3] = fmaf(d1, c[3], part[3]);
+    }
 }
 
 }  // namespace pn

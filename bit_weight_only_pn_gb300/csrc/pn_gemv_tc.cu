@@ -36,8 +36,6 @@
 //    starts from zero and is scaled by its d in fp32, so every product is
 //    exact and every sum is an fp32 sum.
 #include <cstdint>
-#include <type_traits>
-#include <utility>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -139,15 +137,6 @@ __device__ __forceinline__ bool slot_work(const Batch& b, int c, int p, int& j, 
     const int cs = j == 0 ? b.cs0 : 0;
     const int ce = j == b.nt - 1 ? b.ce_last : b.chunks;
     return chunk >= cs && chunk < ce;
-}
-
-template <int N, typename Fn, int... I>
-__device__ __forceinline__ void static_for_impl(Fn&& fn, std::integer_sequence<int, I...>) {
-    (fn(std::integral_constant<int, I>{}), ...);
-}
-template <int N, typename Fn>
-__device__ __forceinline__ void static_for(Fn&& fn) {
-    static_for_impl<N>(fn, std::make_integer_sequence<int, N>{});
 }
 
 // First unit of CTA c's range.
@@ -281,43 +270,6 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
 
 // ----------------------------------------------------------------- decode --
 
-// Fragment row g (and g + 8) of a tile reads staged row tile_row(g) (and +8).
-// Rows land 272 bytes (68 banks, 4 mod 32) apart; taking the even rows for
-// g = 0..3 and the odd rows for g = 4..7 makes every 64-bit load of a
-// half-warp hit 32 distinct banks.
-__device__ __forceinline__ int tile_row(int g) { return ((g & 3) << 1) | (g >> 2); }
-
-// Loads code words 2t and 2t+1 of block B of a staged row (8-byte aligned).
-template <int B>
-__device__ __forceinline__ void load_words(const uint8_t* row, int t, uint32_t& w0, uint32_t& w1) {
-    constexpr int kOff = B * kBlockBytes;
-    if constexpr (B % 2 == 0) {
-        // block starts 4-byte aligned: its words start 2 bytes into aligned words
-        const uint8_t* a = row + kOff + 8 * t;
-        uint32_t v0, v1, v2;
-        if constexpr (kOff % 8 == 0) {
-            const uint2 p = lds_u64(a);
-            v0 = p.x; v1 = p.y; v2 = lds_u32(a + 8);
-        } else {
-            v0 = lds_u32(a);
-            const uint2 p = lds_u64(a + 4);
-            v1 = p.x; v2 = p.y;
-        }
-        w0 = realign16(v0, v1);
-        w1 = realign16(v1, v2);
-    } else {
-        // block starts 2 bytes past a 4-byte boundary: its words are aligned
-        const uint8_t* a = row + kOff + 2 + 8 * t;
-        if constexpr ((kOff + 2) % 8 == 0) {
-            const uint2 p = lds_u64(a);
-            w0 = p.x; w1 = p.y;
-        } else {
-            w0 = lds_u32(a);
-            w1 = lds_u32(a + 4);
-        }
-    }
-}
-
 // x pairs for code words 2t (xb[0..P-1]) and 2t+1 (xb[P..2P-1]) of block B.
 template <int TYPE, int B>
 __device__ __forceinline__ void load_x(const uint8_t* xrow, int t, uint32_t (&xb)[2 * Format<TYPE>::kPairs]) {
@@ -354,29 +306,9 @@ __device__ __forceinline__ void mma_tile_half(const uint8_t* tile, const uint8_t
     float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     static_for<kWarpBlocks>([&](auto bc) {
         constexpr int B = H * kWarpBlocks + decltype(bc)::value;
-        const float d0 = lds_half_as_float(r0 + B * kBlockBytes);
-        const float d1 = lds_half_as_float(r1 + B * kBlockBytes);
-        uint32_t w00, w10, w01, w11;        // w<word><row>: words 2t / 2t+1 of rows g / g+8
-        load_words<B>(r0, t, w00, w10);
-        load_words<B>(r1, t, w01, w11);
-        const uint32_t s00 = w00 >> F::kHighShift, s10 = w10 >> F::kHighShift;
-        const uint32_t s01 = w01 >> F::kHighShift, s11 = w11 >> F::kHighShift;
         uint32_t xb[2 * F::kPairs];
         load_x<TYPE, B>(xrow, t, xb);
-        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        static_for<F::kPairs>([&](auto pc) {
-            constexpr int P = decltype(pc)::value;
-            const uint32_t a[4] = {
-                decode_pair<TYPE, P>(w00, s00),   // row g,   k = 2t, 2t+1   <- word 2t
-                decode_pair<TYPE, P>(w01, s01),   // row g+8, k = 2t, 2t+1   <- word 2t
-                decode_pair<TYPE, P>(w10, s10),   // row g,   k = 2t+8, 2t+9 <- word 2t+1
-                decode_pair<TYPE, P>(w11, s11)};  // row g+8, k = 2t+8, 2t+9 <- word 2t+1
-            mma_16816(c, a, xb[P], xb[F::kPairs + P], c);
-        });
-        part[0] = fmaf(d0, c[0], part[0]);
-        part[1] = fmaf(d0, c[1], part[1]);
-        part[2] = fmaf(d1, c[2], part[2]);
-        part[3] = fmaf(d1, c[3], part[3]);
+        block_mma<TYPE, B>(r0, r1, t, xb, part);
     });
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += part[i];
@@ -811,7 +743,7 @@ WorkspaceLayout workspace_layout(int64_t /*total_tiles*/, int max_ctas) {
     return L;
 }
 
-int tc_max_ctas(int num_sms) { return num_sms; }
+int tc_max_ctas(int num_sms) { return warp_max_ctas(num_sms); }
 
 cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, void* workspace,
                            size_t workspace_bytes, int num_sms, uint64_t timeout_ns, int stall,

@@ -40,6 +40,15 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, void* workspac
                            size_t workspace_bytes, int num_sms, uint64_t timeout_ns, int stall,
                            cudaStream_t s, int* needs_bytes_out);
 
+// Most thread blocks any tensor-core GEMV launch uses; the workspace holds a
+// boundary slot pair for each.
 int tc_max_ctas(int num_sms);
+
+// Tensor-core GEMV for M <= 2 in which every warp streams its own units
+// (same eligibility, same workspace layout as launch_gemv_tc).
+cudaError_t launch_gemv_warp(const GemvTensor* t, int count, int M, void* workspace,
+                             size_t workspace_bytes, int num_sms, uint64_t timeout_ns, int stall,
+                             cudaStream_t s, int* needs_bytes_out);
+int warp_max_ctas(int num_sms);
 
 }  // namespace pn

@@ -26,10 +26,10 @@
 
 namespace {
 
-// Room for the workspace of a device with up to 253 SMs: the workspace size
-// depends only on the SM count s, 256 + 1024 * (s + 1) bytes plus the
-// (s + 1) counters rounded up to 256 bytes.
-constexpr size_t kNoAllocScratchBytes = 256 * 1024;
+// Room for the workspace of a device with up to 254 SMs: the workspace size
+// depends only on the SM count s, 256 + 1024 * (2s + 1) bytes plus the
+// (2s + 1) counters rounded up to 256 bytes.
+constexpr size_t kNoAllocScratchBytes = 512 * 1024;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
