@@ -731,15 +731,17 @@ bool encode_x(CUtensorMap* map, const GemvTensor& t, int M) {
 
 }  // namespace
 
-// Workspace: status word, then for every CTA boundary (one more than the
-// largest grid) a counter and two partial-sum slots.
+// Workspace: status word, then for every thread-block boundary (one more
+// than the largest grid) two partial-sum slots and a counter (batch kernel)
+// and one row of tagged words (warp kernel).
 WorkspaceLayout workspace_layout(int64_t /*total_tiles*/, int max_ctas) {
     WorkspaceLayout L;
     L.status = 0;
     L.partials = 256;
     const size_t boundaries = static_cast<size_t>(max_ctas) + 1;
     L.counters = L.partials + boundaries * 2 * kSlotFloats * sizeof(float);
-    L.total = L.counters + ((boundaries * 4 + 255) / 256) * 256;
+    L.tagged = L.counters + ((boundaries * 4 + 255) / 256) * 256;
+    L.total = L.tagged + boundaries * kTileRows * 2 * sizeof(uint64_t);
     return L;
 }
 

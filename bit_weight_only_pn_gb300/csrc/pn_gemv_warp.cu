@@ -12,21 +12,23 @@
 //    are numbered tile-major over every tensor of the call.  The grid (two
 //    thread blocks per SM) splits them into equal contiguous ranges of at
 //    least one tile each, so a tile is shared by at most two blocks.
-//  * A block has seven compute warps and one epilogue warp.  The compute warps
-//    split the block's units into equal contiguous shares of one sequence
-//    that starts with the parts of the two tiles cut by the block's
-//    boundaries, so those parts are finished first.  No compute warp ever
-//    waits for another.
-//  * Each compute warp owns a three-stage shared-memory ring: lane 0 issues
-//    one 2-D TMA box (16 rows x 272 bytes) per unit, completing on the stage's
+//  * A block's eight warps split its units into equal contiguous shares of
+//    one sequence that starts with the block's parts of the two tiles cut by
+//    its boundaries, so those parts are finished first.  No warp ever waits
+//    for another while it streams.
+//  * Each warp owns a three-stage shared-memory ring: lane 0 issues one 2-D
+//    TMA box (16 rows x 272 bytes) per unit, completing on the stage's
 //    mbarrier, and the warp decodes one stage while the next two are in
 //    flight.  x is read through L1, prefetched one unit ahead.
-//  * A tile that one warp covers completely is stored at once.  The epilogue
-//    warp adds the warps' parts of the other tiles in warp order; for a tile
-//    cut by a block boundary it deposits the block's part in the workspace
-//    while the compute warps are still busy, and the second of the two blocks
-//    to get there adds left part + right part, so results do not depend on
-//    timing and the slow global hand-off stays off the kernel's tail.
+//  * A tile that one warp covers completely is stored at once.  The parts of
+//    a tile split between warps go to shared memory; the last warp to finish
+//    its part (a shared-memory counter) adds them in warp order.  A tile cut
+//    by a block boundary is finished by the block holding its first chunks:
+//    the other block stores its part as 64-bit {value, tag} words, which are
+//    single-copy atomic and need no fence, and the first block picks them up
+//    with loads it checks only after decoding its next unit, adds first part
+//    + second part, stores, and clears the tags.  Results do not depend on
+//    timing, and no fence, atomic or global round trip sits on the tail.
 //  * Programmatic dependent launch: the kernel lets the next kernel on the
 //    stream launch at once, prefetches its first units into L2, and only then
 //    waits for the previous kernel to complete; W, x and the workspace are
@@ -45,9 +47,8 @@
 namespace pn {
 namespace {
 
-constexpr int kComputeWarps = 7;
-constexpr int kEpilogueWarp = kComputeWarps;
-constexpr int kThreads = (kComputeWarps + 1) * 32;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
 constexpr int kCtasPerSm = 2;
 constexpr int kStages = 3;
 constexpr int kTileRows = 16;
@@ -57,22 +58,25 @@ constexpr int kBoxWords = kChunkBytes / 4;                // TMA box inner exten
 constexpr int kUnitBytes = kTileRows * kChunkBytes;       // 4352
 constexpr int kWarpMaxM = 2;
 constexpr int kRecFloats = kTileRows * kWarpMaxM;         // one part of a tile: [row][token]
-// Tile parts a compute warp hands to the epilogue warp: its part of the
-// left-cut tile, of the right-cut tile, and of the first and last tiles of its
-// share of the middle when it does not cover them completely.
-constexpr int kRecLeft = 0, kRecRight = 1, kRecMidFirst = 2, kRecMidLast = 3, kRecs = 4;
-constexpr int kRingBytes = kComputeWarps * kStages * kUnitBytes;
-constexpr int kRecOffset = kRingBytes;                                           // [warp][kRecs][kRecFloats]
-constexpr int kKeyOffset = kRecOffset + kComputeWarps * kRecs * kRecFloats * 4;  // [warp][2] int64 (middle records)
-constexpr int kBarOffset = kKeyOffset + kComputeWarps * 2 * 8;                  // [warp][stage], then left, right, done
-constexpr int kSmemBytes = kBarOffset + (kComputeWarps * kStages + 3) * 8;
+// Segments of a block's sequence: its part of the tile cut by its left
+// boundary, its part of the tile cut by its right boundary, the whole tiles
+// in between.
+constexpr int kSegLeft = 0, kSegRight = 1, kSegMid = 2;
+// Per warp, two tile parts: [0] its part of a tile an earlier warp began,
+// [1] its part of a tile it begins itself.
+constexpr int kRingBytes = kWarps * kStages * kUnitBytes;
+constexpr int kRecOffset = kRingBytes;                                  // [warp][2][kRecFloats] float
+constexpr int kCntOffset = kRecOffset + kWarps * 2 * kRecFloats * 4;    // [warp] uint32: parts in, per begun tile
+constexpr int kBarOffset = kCntOffset + kWarps * 4;                     // [warp][stage] mbarrier
+constexpr int kSmemBytes = kBarOffset + kWarps * kStages * 8;
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                    // PN_ETIMEOUT
-constexpr int kSlotFloats = kTileRows * kMaxM;            // one boundary slot (shared layout)
+constexpr uint32_t kTagFull = 1u;                         // tag of a deposited part word
 
 static_assert(kStagedRowBytes == kChunkBytes, "staged rows are one chunk wide");
 static_assert(kUnitBytes % 128 == 0, "every stage starts 128-byte aligned");
 static_assert(kSmemBytes <= 110 * 1024, "two thread blocks fit on one SM");
+static_assert(kCntOffset % 8 == 0 && kBarOffset % 8 == 0, "aligned bookkeeping");
 
 struct WTensor {
     const uint16_t* x;
@@ -91,10 +95,9 @@ struct WarpParams {
     int count;
     int M;
     int grid;
-    uint32_t units;                // units * grid < 2^32 and units * 8 < 2^32 (checked on the host)
+    uint32_t units;                // units * grid < 2^32 and units * 8 < 2^29 (checked on the host)
     uint32_t* status;
-    uint32_t* counters;            // one per thread-block boundary
-    float* partials;               // [boundary][side][kSlotFloats]
+    uint64_t* tagged;              // [boundary][kRecFloats] {value bits, tag}
     uint64_t timeout_ns;
     int stall_first_step;          // testing aid: see pn_set_test_stall
 };
@@ -116,7 +119,6 @@ struct Cursor {
             if (++tile == P.t[e].tiles) { tile = 0; ++e; }
         }
     }
-    __device__ int64_t key() const { return (static_cast<int64_t>(e) << 32) | static_cast<uint32_t>(tile); }
 };
 
 __device__ __forceinline__ uint32_t range_start(const WarpParams& P, int c) {
@@ -186,21 +188,6 @@ __device__ __forceinline__ void unit_mma(const uint8_t* tile, const uint16_t* xc
     for (int i = 0; i < 4; ++i) acc[i] += part[i];
 }
 
-// Stores a whole tile from the accumulator fragments (lanes t = 0 hold the
-// columns of tokens 0 and 1).
-__device__ __forceinline__ void store_tile(const WTensor& T, int M, int tile, int lane, const float (&v)[4]) {
-    if ((lane & 3) != 0) return;
-    const int row0 = tile * kTileRows + tile_row(lane >> 2);
-    const int rows[2] = {row0, row0 + 8};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        if (rows[h] < T.N) {
-            T.y[rows[h]] = v[2 * h];
-            if (M > 1) T.y[static_cast<int64_t>(T.N) + rows[h]] = v[2 * h + 1];
-        }
-    }
-}
-
 // Writes a tile part into record r of this warp: [row][token].
 __device__ __forceinline__ void put_record(float* rec, int lane, const float (&v)[4]) {
     if ((lane & 3) != 0) return;
@@ -211,54 +198,82 @@ __device__ __forceinline__ void put_record(float* rec, int lane, const float (&v
     rec[(row + 8) * kWarpMaxM + 1] = v[3];
 }
 
-__device__ __forceinline__ float* slot_ptr(const WarpParams& P, int boundary, int side) {
-    return P.partials + (static_cast<int64_t>(boundary) * 2 + side) * kSlotFloats;
-}
-
-// A finished block-level sum of one tile, one value per lane: lane = row * 2 + token.
-// `cut` is 0 for a tile wholly inside this block, 1 for the tile cut by the
-// block's left boundary, 2 for the one cut by its right boundary.
-__device__ void emit_tile(const WarpParams& P, int64_t key, float v, int cut, int lane) {
-    const int e = static_cast<int>(key >> 32), tile = static_cast<int>(key & 0xFFFFFFFF);
-    const WTensor& T = P.t[e];
-    const int row = tile * kTileRows + (lane >> 1), m = lane & 1;
-    if (cut != 0) {
-        // our part is side 1 of boundary blockIdx.x (left cut) or side 0 of
-        // boundary blockIdx.x + 1 (right cut); the second arriver adds both
-        const int boundary = blockIdx.x + (cut == 2 ? 1 : 0);
-        const int side = cut == 1 ? 1 : 0;
-        __stcg(slot_ptr(P, boundary, side) + (lane >> 1) * kMaxM + m, v);
-        __threadfence();
-        __syncwarp();
-        uint32_t old = 0;
-        if (lane == 0) old = atomicAdd(P.counters + boundary, 1u);
-        old = __shfl_sync(0xFFFFFFFFu, old, 0);
-        if (old != 1u) return;
-        __threadfence();
-        const float o = __ldcg(slot_ptr(P, boundary, side ^ 1) + (lane >> 1) * kMaxM + m);
-        v = side == 1 ? o + v : v + o;           // left part + right part
-        if (lane == 0) atomicExch(P.counters + boundary, 0u);
-    }
+// Stores a finished tile sum held one value per lane: lane = row * 2 + token.
+__device__ __forceinline__ void store_lanes(const WarpParams& P, const Cursor& c, float v, int lane) {
+    const WTensor& T = P.t[c.e];
+    const int row = c.tile * kTileRows + (lane >> 1), m = lane & 1;
     if (row < T.N && m < P.M) T.y[static_cast<int64_t>(m) * T.N + row] = v;
 }
 
-// A compute warp's share of its block's units: up to three runs of
-// consecutive units (left-cut part, right-cut part, middle), walked in order.
-// The runs are kept in scalars (run 0 is the current one) so that nothing
-// is indexed at run time.
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// This block's part of the tile cut by its left boundary (the tile's later
+// chunks), left for the previous block as {value bits, tag} words.
+__device__ __forceinline__ void deposit(const WarpParams& P, float v, int lane) {
+    st_relaxed_u64(P.tagged + static_cast<int64_t>(blockIdx.x) * kRecFloats + lane,
+                   (static_cast<uint64_t>(kTagFull) << 32) | __float_as_uint(v));
+}
+
+// The tile cut by this block's right boundary: this block holds its first
+// chunks and finishes it once the next block's part has arrived.  poll()
+// checks the words loaded by the previous poll (issued at least one unit of
+// decoding earlier) and loads them again while they are not all tagged.
+struct Finisher {
+    bool pending = false;
+    float mine = 0.0f;         // this block's part (first chunks), lane = row * 2 + token
+    uint64_t seen = 0;         // the word last loaded
+    uint64_t t0 = 0;
+    Cursor tile{0, 0, 0};
+    __device__ uint64_t* word(const WarpParams& P, int lane) const {
+        return P.tagged + static_cast<int64_t>(blockIdx.x + 1) * kRecFloats + lane;
+    }
+    __device__ void start(const WarpParams& P, const Cursor& c, float v, int lane) {
+        pending = true;
+        mine = v;
+        tile = c;
+        seen = ld_relaxed_u64(word(P, lane));
+        t0 = globaltimer_ns();
+    }
+    __device__ void poll(const WarpParams& P, int lane) {
+        if (!pending) return;
+        if (__all_sync(0xFFFFFFFFu, static_cast<uint32_t>(seen >> 32) == kTagFull)) {
+            store_lanes(P, tile, mine + __uint_as_float(static_cast<uint32_t>(seen)), lane);  // first + second part
+            st_relaxed_u64(word(P, lane), 0ull);
+            pending = false;
+        } else if (globaltimer_ns() - t0 > P.timeout_ns) {
+            if (lane == 0) atomicCAS(P.status, 0u, kStatusTimeout);
+            pending = false;
+        } else {
+            seen = ld_relaxed_u64(word(P, lane));
+        }
+    }
+};
+
+// A warp's share of its block's units: up to three runs of consecutive units
+// (left-cut part, right-cut part, middle), walked in order.  The runs are kept
+// in scalars (run 0 is the current one) so that nothing is indexed at run time.
 struct Walk {
-    uint32_t a0, b0, a1, b1, a2, b2;   // runs [a, b)
-    int k0, k1, k2;                    // their kinds: kRecLeft, kRecRight, kRecMidFirst
+    uint32_t a0, b0, a1, b1, a2, b2;   // runs [a, b) of units
+    uint32_t q0, q1, q2;               // sequence position of each run's first unit
+    int k0, k1, k2;                    // their segments: kSegLeft, kSegRight, kSegMid
     uint32_t u;                        // current unit, in run 0
     Cursor c;                          // its position
-    __device__ void init() { a0 = b0 = a1 = b1 = a2 = b2 = 0; k0 = k1 = k2 = 0; }
-    __device__ void add(uint32_t a, uint32_t b, int k) {
+    __device__ void init() { a0 = b0 = a1 = b1 = a2 = b2 = 0; q0 = q1 = q2 = 0; k0 = k1 = k2 = 0; }
+    __device__ void add(uint32_t a, uint32_t b, uint32_t q, int k) {
         if (a >= b) return;
-        if (a0 == b0) { a0 = a; b0 = b; k0 = k; }
-        else if (a1 == b1) { a1 = a; b1 = b; k1 = k; }
-        else { a2 = a; b2 = b; k2 = k; }
+        if (a0 == b0) { a0 = a; b0 = b; q0 = q; k0 = k; }
+        else if (a1 == b1) { a1 = a; b1 = b; q1 = q; k1 = k; }
+        else { a2 = a; b2 = b; q2 = q; k2 = k; }
     }
     __device__ bool valid() const { return a0 < b0; }
+    __device__ uint32_t pos() const { return q0 + (u - a0); }
     __device__ void start(const WarpParams& P) {
         u = a0;
         if (valid()) c.locate(P, u);
@@ -268,16 +283,50 @@ struct Walk {
             c.next(P);
             return;
         }
-        a0 = a1; b0 = b1; k0 = k1;
-        a1 = a2; b1 = b2; k1 = k2;
+        a0 = a1; b0 = b1; q0 = q1; k0 = k1;
+        a1 = a2; b1 = b2; q1 = q2; k1 = k2;
         a2 = b2 = 0;
         start(P);
     }
 };
 
-// Whether [p0, p1) and [lo, hi) share a position.
-__device__ __forceinline__ bool meets(uint32_t p0, uint32_t p1, uint32_t lo, uint32_t hi) {
-    return max(p0, lo) < min(p1, hi);
+// The warp whose share [n w / 8, n (w + 1) / 8) holds sequence position pos.
+__device__ __forceinline__ int warp_of(uint32_t pos, uint32_t n) {
+    return min(static_cast<int>((pos * kWarps + kWarps - 1) / n), kWarps - 1);
+}
+
+// Accumulator fragments (lanes t = 0 hold rows tile_row(g), +8) as one value
+// per lane, lane = row * 2 + token.
+__device__ __forceinline__ float to_lanes(const float (&acc)[4], int lane) {
+    const int row = lane >> 1, m = lane & 1, r = row & 7;
+    const int src = (((r & 1) << 2) | (r >> 1)) << 2;      // lane g * 4 with tile_row(g) == r
+    const float v0 = __shfl_sync(0xFFFFFFFFu, acc[0], src), v1 = __shfl_sync(0xFFFFFFFFu, acc[1], src);
+    const float v2 = __shfl_sync(0xFFFFFFFFu, acc[2], src), v3 = __shfl_sync(0xFFFFFFFFu, acc[3], src);
+    return row < 8 ? (m ? v1 : v0) : (m ? v3 : v2);
+}
+
+// This warp's part of a tile split between warps wa..wb (wa < wb).  The part goes to shared memory; the last warp
+// to deliver its part gets true and the tile sum in warp order, one value per
+// lane (lane = row * 2 + token).
+__device__ bool hand_in(uint8_t* smem, int warp, int lane, int wa, int wb, uint32_t n, const float (&acc)[4],
+                        float& sum) {
+    float* recs = reinterpret_cast<float*>(smem + kRecOffset);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + kCntOffset);
+    put_record(recs + (warp * 2 + (warp == wa ? 1 : 0)) * kRecFloats, lane, acc);
+    // contributors: the warps of wa..wb whose share is not empty
+    uint32_t parts = 0;
+    for (int w = wa; w <= wb; ++w) parts += (n * (w + 1) / kWarps > n * w / kWarps) ? 1u : 0u;
+    __threadfence_block();
+    __syncwarp();
+    uint32_t old = 0;
+    if (lane == 0) old = atomicAdd(cnt + wa, 1u);
+    old = __shfl_sync(0xFFFFFFFFu, old, 0);
+    if (old + 1 != parts) return false;
+    __threadfence_block();
+    sum = recs[(wa * 2 + 1) * kRecFloats + lane];
+    for (int w = wa + 1; w <= wb; ++w)
+        if (n * (w + 1) / kWarps > n * w / kWarps) sum += recs[(w * 2) * kRecFloats + lane];
+    return true;
 }
 
 // Prefetches into L1 the chunk of x that unit `c` reads, one line per lane
@@ -290,11 +339,6 @@ __device__ __forceinline__ void prefetch_x(const WarpParams& P, const Cursor& c,
         prefetch_l1(T.x + static_cast<int64_t>(m) * T.K + c.chunk * kChunkBlocks * per_block(T.type) + l * 64);
 }
 
-__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar);
-}
-
 template <bool M1>
 __device__ __forceinline__ void compute_unit(const WTensor& T, const uint8_t* stage, const uint16_t* xc, int lane,
                                              float (&acc)[4]) {
@@ -304,23 +348,24 @@ __device__ __forceinline__ void compute_unit(const WTensor& T, const uint8_t* st
 
 template <bool M1>
 __device__ void compute_warp(const WarpParams& P, uint8_t* smem, int warp, int lane, uint32_t c0, uint32_t n,
-                             uint32_t nl, uint32_t nr, uint32_t bar_left, uint32_t bar_right, uint32_t bar_done) {
-    const uint32_t p0 = n * static_cast<uint32_t>(warp) / kComputeWarps;
-    const uint32_t p1 = n * static_cast<uint32_t>(warp + 1) / kComputeWarps;
+                             uint32_t nl, uint32_t nr, const Cursor& left_tile, const Cursor& right_tile) {
+    const uint32_t p0 = n * static_cast<uint32_t>(warp) / kWarps;
+    const uint32_t p1 = n * static_cast<uint32_t>(warp + 1) / kWarps;
     // sequence position -> unit: [0, nl) left-cut part, [nl, nl + nr) right-cut
     // part (the block's last nr units), [nl + nr, n) the middle
     Walk w;
     w.init();
-    w.add(c0 + min(p0, nl), c0 + min(p1, nl), kRecLeft);
-    w.add(c0 + n - nr + (min(max(p0, nl), nl + nr) - nl), c0 + n - nr + (min(max(p1, nl), nl + nr) - nl), kRecRight);
-    w.add(c0 + nl + (max(p0, nl + nr) - nl - nr), c0 + nl + (max(p1, nl + nr) - nl - nr), kRecMidFirst);
-    const bool in_left = meets(p0, p1, 0, nl), in_right = meets(p0, p1, nl, nl + nr);
-
+    {
+        const uint32_t l0 = min(p0, nl), l1 = min(p1, nl);
+        const uint32_t r0 = min(max(p0, nl), nl + nr), r1 = min(max(p1, nl), nl + nr);
+        const uint32_t m0 = max(p0, nl + nr), m1 = max(p1, nl + nr);
+        w.add(c0 + l0, c0 + l1, l0, kSegLeft);
+        w.add(c0 + n - nr + (r0 - nl), c0 + n - nr + (r1 - nl), r0, kSegRight);
+        w.add(c0 + nl + (m0 - nl - nr), c0 + nl + (m1 - nl - nr), m0, kSegMid);
+    }
     const uint32_t ring = smem_addr(smem) + warp * kStages * kUnitBytes;
     const uint8_t* ring_p = smem + warp * kStages * kUnitBytes;
     const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;
-    float* recs = reinterpret_cast<float*>(smem + kRecOffset) + warp * kRecs * kRecFloats;
-    int64_t* keys = reinterpret_cast<int64_t*>(smem + kKeyOffset) + warp * 2;
 
     Walk iss = w;
     iss.start(P);
@@ -358,9 +403,7 @@ __device__ void compute_warp(const WarpParams& P, uint8_t* smem, int warp, int l
     cur.start(P);
     const int token = min(lane >> 2, P.M - 1);   // this lane's B column (columns past M repeat token M-1)
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    bool from_start = false;                      // the open middle tile began at chunk 0 in this warp
-    bool mid_first = true;                        // no middle record written yet
-    bool arrived_left = false, arrived_right = false;
+    Finisher fin;
     int done = 0;
     while (cur.valid()) {
         const int s = done % kStages;
@@ -369,8 +412,6 @@ __device__ void compute_warp(const WarpParams& P, uint8_t* smem, int warp, int l
             break;
         }
         const WTensor& T = P.t[cur.c.e];
-        const int kind = cur.k0;
-        if (kind == kRecMidFirst && (cur.u == cur.a0 || cur.c.chunk == 0)) from_start = cur.c.chunk == 0;
         const uint16_t* xc = T.x + static_cast<int64_t>(token) * T.K + cur.c.chunk * kChunkBlocks * per_block(T.type);
         compute_unit<M1>(T, ring_p + s * kUnitBytes, xc, lane, acc);
         __syncwarp();
@@ -379,25 +420,24 @@ __device__ void compute_warp(const WarpParams& P, uint8_t* smem, int warp, int l
             issue(s);
         }
         ++done;
+        fin.poll(P, lane);                        // words loaded one unit ago
+        // the end of this warp's part of a tile?
+        const int seg = cur.k0;
         const bool run_end = cur.u + 1 == cur.b0;
         const bool last_chunk = cur.c.chunk == T.chunks - 1;
-        if (kind != kRecMidFirst) {
-            if (run_end) {                        // this warp's part of a cut tile
-                put_record(recs + kind * kRecFloats, lane, acc);
-                if (kind == kRecLeft) { warp_arrive(bar_left, lane); arrived_left = true; }
-                else { warp_arrive(bar_right, lane); arrived_right = true; }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] = 0.0f;
+        if (run_end || (seg == kSegMid && last_chunk)) {
+            const uint32_t pos = cur.pos();
+            const uint32_t ts = seg == kSegLeft ? 0u : seg == kSegRight ? nl : pos - cur.c.chunk;
+            const uint32_t te = seg == kSegLeft ? nl : seg == kSegRight ? nl + nr : ts + T.chunks;
+            const int wa = warp_of(ts, n), wb = warp_of(te - 1, n);
+            float v = 0.0f;
+            const bool whole = wa == wb;
+            if (whole) v = to_lanes(acc, lane);
+            if (whole || hand_in(smem, warp, lane, wa, wb, n, acc, v)) {
+                if (seg == kSegLeft) deposit(P, v, lane);
+                else if (seg == kSegRight) fin.start(P, right_tile, v, lane);
+                else store_lanes(P, cur.c, v, lane);
             }
-        } else if (last_chunk || run_end) {
-            if (from_start && last_chunk) {
-                store_tile(T, P.M, cur.c.tile, lane, acc);
-            } else {
-                const int r = mid_first ? kRecMidFirst : kRecMidLast;
-                put_record(recs + r * kRecFloats, lane, acc);
-                if (lane == 0) keys[r - kRecMidFirst] = cur.c.key();
-            }
-            mid_first = false;
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = 0.0f;
         }
@@ -410,61 +450,11 @@ __device__ void compute_warp(const WarpParams& P, uint8_t* smem, int warp, int l
             wait_bounded(bar0 + 8 * (k % kStages), static_cast<uint32_t>(k / kStages) & 1u, kDrainLimitNs);
         }
     }
-    if (in_left && !arrived_left) warp_arrive(bar_left, lane);
-    if (in_right && !arrived_right) warp_arrive(bar_right, lane);
-    warp_arrive(bar_done, lane);
-}
-
-// Number of compute warps whose share of an n-unit sequence meets [lo, hi).
-__device__ __forceinline__ int warps_meeting(uint32_t n, uint32_t lo, uint32_t hi) {
-    int k = 0;
-#pragma unroll
-    for (int w = 0; w < kComputeWarps; ++w)
-        k += meets(n * w / kComputeWarps, n * (w + 1) / kComputeWarps, lo, hi) ? 1 : 0;
-    return k;
-}
-
-// The epilogue warp: finishes the block's two cut tiles as soon as the
-// compute warps have their parts, then the tiles split between compute warps.
-__device__ void epilogue_warp(const WarpParams& P, const uint8_t* smem, int lane, uint32_t c0, uint32_t n,
-                              uint32_t nl, uint32_t nr, const Cursor& first, const Cursor& last,
-                              uint32_t bar_left, uint32_t bar_right, uint32_t bar_done) {
-    const float* recs = reinterpret_cast<const float*>(smem + kRecOffset);
-    const int64_t* keys = reinterpret_cast<const int64_t*>(smem + kKeyOffset);
-    for (int side = 0; side < 2; ++side) {
-        const uint32_t lo = side == 0 ? 0 : nl, hi = side == 0 ? nl : nl + nr;
-        if (lo == hi) continue;
-        if (!warp_wait(side == 0 ? bar_left : bar_right, 0u, P.timeout_ns, lane)) {
-            if (lane == 0) atomicCAS(P.status, 0u, kStatusTimeout);
-            return;
-        }
-        float v = 0.0f;
-        for (int w = 0; w < kComputeWarps; ++w) {
-            if (meets(n * w / kComputeWarps, n * (w + 1) / kComputeWarps, lo, hi)) v += recs[(w * kRecs + (side == 0 ? kRecLeft : kRecRight)) * kRecFloats + lane];
-        }
-        emit_tile(P, side == 0 ? first.key() : last.key(), v, side == 0 ? 1 : 2, lane);
+    while (fin.pending) {
+        __nanosleep(64);
+        fin.poll(P, lane);
     }
-    if (!warp_wait(bar_done, 0u, P.timeout_ns, lane)) {
-        if (lane == 0) atomicCAS(P.status, 0u, kStatusTimeout);
-        return;
-    }
-    int64_t run_key = -1;
-    float run = 0.0f;
-    for (int r = 0; r < 2 * kComputeWarps; ++r) {
-        const int w = r >> 1, k = r & 1;
-        const int64_t key = keys[w * 2 + k];
-        if (key < 0) continue;
-        const float v = recs[(w * kRecs + kRecMidFirst + k) * kRecFloats + lane];
-        if (key == run_key) {
-            run += v;
-        } else {
-            if (run_key >= 0) emit_tile(P, run_key, run, 0, lane);
-            run_key = key;
-            run = v;
-        }
-    }
-    if (run_key >= 0) emit_tile(P, run_key, run, 0, lane);
-    (void)c0;
+    (void)left_tile;
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_warp_kernel(const __grid_constant__ WarpParams P) {
@@ -482,30 +472,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_warp_kernel(const _
     // the one it shares with the next block
     const uint32_t nl = (n > 0 && first.chunk != 0) ? static_cast<uint32_t>(P.t[first.e].chunks - first.chunk) : 0u;
     const uint32_t nr = (n > 0 && last.chunk != P.t[last.e].chunks - 1) ? static_cast<uint32_t>(last.chunk + 1) : 0u;
-    const uint32_t bars = smem_addr(smem + kBarOffset) + kComputeWarps * kStages * 8;
-    const uint32_t bar_left = bars, bar_right = bars + 8, bar_done = bars + 16;
-    if (threadIdx.x == 0) {
-        const int kl = warps_meeting(n, 0, nl), kr = warps_meeting(n, nl, nl + nr);
-        mbar_init(bar_left, kl > 0 ? kl : 1);
-        mbar_init(bar_right, kr > 0 ? kr : 1);
-        mbar_init(bar_done, kComputeWarps);
-    }
-    if (warp < kComputeWarps && lane == 0) {
+    if (lane == 0) {
         const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;
         for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
-        int64_t* keys = reinterpret_cast<int64_t*>(smem + kKeyOffset) + warp * 2;
-        keys[0] = -1;
-        keys[1] = -1;
+        reinterpret_cast<uint32_t*>(smem + kCntOffset)[warp] = 0u;
     }
     __syncthreads();
-    if (warp != kEpilogueWarp) {
-        if (P.M == 1) compute_warp<true>(P, smem, warp, lane, c0, n, nl, nr, bar_left, bar_right, bar_done);
-        else compute_warp<false>(P, smem, warp, lane, c0, n, nl, nr, bar_left, bar_right, bar_done);
-    } else {
-        griddep_wait();
-        epilogue_warp(P, smem, lane, c0, n, nl, nr, first, last, bar_left, bar_right, bar_done);
-    }
+    if (P.M == 1) compute_warp<true>(P, smem, warp, lane, c0, n, nl, nr, first, last);
+    else compute_warp<false>(P, smem, warp, lane, c0, n, nl, nr, first, last);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -570,7 +545,7 @@ cudaError_t launch_gemv_warp(const GemvTensor* t, int count, int M, void* worksp
     uint64_t grid = units / static_cast<uint64_t>(max_chunks);
     if (grid > static_cast<uint64_t>(warp_max_ctas(num_sms))) grid = warp_max_ctas(num_sms);
     if (grid < 1) grid = 1;
-    if (units * grid >= (1ull << 32) || units * kComputeWarps >= (1ull << 32)) return cudaErrorInvalidValue;
+    if (units * grid >= (1ull << 32) || units * kWarps >= (1ull << 32)) return cudaErrorInvalidValue;
     P.grid = static_cast<int>(grid);
     P.units = static_cast<uint32_t>(units);
     const WorkspaceLayout L = workspace_layout(0, tc_max_ctas(num_sms));
@@ -581,8 +556,7 @@ cudaError_t launch_gemv_warp(const GemvTensor* t, int count, int M, void* worksp
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     P.status = reinterpret_cast<uint32_t*>(ws + L.status);
-    P.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
-    P.partials = reinterpret_cast<float*>(ws + L.partials);
+    P.tagged = reinterpret_cast<uint64_t*>(ws + L.tagged);
     P.timeout_ns = timeout_ns;
     P.stall_first_step = stall;
 

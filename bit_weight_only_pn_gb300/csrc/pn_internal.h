@@ -28,8 +28,9 @@ cudaError_t launch_gemv_simt(const GemvTensor& t, int M, cudaStream_t s);
 // Workspace layout of the tensor-core GEMV (all offsets in bytes).
 struct WorkspaceLayout {
     size_t status = 0;        // uint32 status word (+ padding to 256)
-    size_t partials = 256;    // float slots, 2 x 8 tiles x 16 rows x 8 tokens per thread block
-    size_t counters = 0;      // uint32 per 16-row tile, after the slots of every possible CTA
+    size_t partials = 256;    // float slots [boundary][side][16 rows x 8 tokens] (batch kernel)
+    size_t counters = 0;      // uint32 per thread-block boundary (batch kernel)
+    size_t tagged = 0;        // 64-bit {value, tag} words [boundary][16 rows x 2 tokens] (warp kernel)
     size_t total = 0;
 };
 WorkspaceLayout workspace_layout(int64_t total_tiles, int max_ctas);

@@ -26,8 +26,8 @@
 
 namespace {
 
-// Room for the workspace of a device with up to 254 SMs: the workspace size
-// depends only on the SM count s, 256 + 1024 * (2s + 1) bytes plus the
+// Room for the workspace of a device with up to 203 SMs: the workspace size
+// depends only on the SM count s: 256 + 1280 * (2s + 1) bytes plus the
 // (2s + 1) counters rounded up to 256 bytes.
 constexpr size_t kNoAllocScratchBytes = 512 * 1024;
 

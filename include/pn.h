@@ -178,7 +178,7 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
  *
  * Scratch: a fixed 512 KiB array in the library's device image, which every
  * GPU that loads the library holds until the process exits.  A device whose
- * workspace (pn_workspace_bytes) would not fit (more than 254 SMs) gets
+ * workspace (pn_workspace_bytes) would not fit (more than 203 SMs) gets
  * PN_EINVAL and nothing is launched.  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress, which may load the
  * library's device module); make that first call before capturing a stream
