@@ -94,25 +94,31 @@ def measured_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of every CUDA source of the library: a recorded ncu traffic figure
+    is only used while the kernels it was taken on are unchanged."""
     h = hashlib.sha256()
-    for f in ("pn_gemv_tc.cu", "pn_device.cuh"):
-        with open(os.path.join(ROOT, "bit_weight_only_pn_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "bit_weight_only_pn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(cfg: int):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "pn_gemv_tc_traffic.md")
+    """Per-launch DRAM bytes (read + write) of the workload's GEMV kernel from
+    the committed ncu summary, if it was taken on the current kernel sources
+    (else None)."""
+    path = os.path.join(ROOT, "profiles", "pn_gemv_traffic.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     want = kernel_source_hash()
-    for m in re.finditer(r"^traffic config=(\d+) bytes_per_launch=(\d+) source=([0-9a-f]+)", text, re.M):
-        if int(m.group(1)) == cfg and m.group(3) == want:
-            return int(m.group(2))
+    for m in re.finditer(r"^traffic config=(\d+) kernel=(\S+) bytes_per_launch=(\d+) source=([0-9a-f]+)",
+                         text, re.M):
+        if int(m.group(1)) == cfg and m.group(4) == want:
+            return int(m.group(3))
     return None
 
 
@@ -184,34 +190,45 @@ class ClockSampler:
 # -------------------------------------------------------------- CPU oracle ---
 
 def oracle_sample_rate(tensors, M, seconds, threads):
-    """Time the CPU oracle on a bounded sample of every tensor's rows; returns
-    (GB/s of algorithmic bytes, description, threads used)."""
+    """Time the CPU oracle on a bounded sample of the workload: a sample of
+    every tensor's rows (all of them when one pass over the whole workload is
+    short), passed over repeatedly for about `seconds` of wall time.  Returns
+    (GB/s of algorithmic bytes, description, threads used, seconds)."""
     import oracle
     from bit_weight_only_pn_gb300 import synth
     o = oracle.Oracle()
-    # calibrate on 64 rows of the first tensor
+    # calibrate on 64 rows of the first tensor (after one untimed call)
     t0, K0, N0 = tensors[0]
-    w = synth.weight_rows(synth.weight_seed(9, 0), N0, K0, range(64))
-    W = o.pack(t0, w)
+    W = o.pack(t0, synth.weight_rows(synth.weight_seed(9, 0), N0, K0, range(64)))
     x = synth.activations(synth.x_seed(9, 0), M, K0)
+    o.gemv(t0, W, K0, x, want_abs=False)
     s = time.perf_counter()
     o.gemv(t0, W, K0, x, want_abs=False)
-    per_row = (time.perf_counter() - s) / 64.0 / max(1, threads) * 1.3
+    per_row = (time.perf_counter() - s) / 64.0 / max(1, threads)
     total_rows = sum(N for _, _, N in tensors)
     frac = min(1.0, seconds / max(per_row * total_rows, 1e-9))
     work = []
     for e, (t, K, N) in enumerate(tensors):
-        rows = max(16, int(N * frac))
-        rows = min(rows, N)
+        rows = min(N, max(16, int(N * frac)))
         w = synth.weight_rows(synth.weight_seed(9, e), N, K, range(rows))
         work.append((t, K, rows, o.pack(t, w), synth.activations(synth.x_seed(9, e), M, K)))
+
+    def one_pass():
+        for t, K, rows, W, x in work:
+            o.gemv_threads(t, W, K, x, threads)
+
     s = time.perf_counter()
-    for t, K, rows, W, x in work:
-        o.gemv_threads(t, W, K, x, threads)
+    one_pass()
+    first = time.perf_counter() - s
+    passes = max(1, int(round(seconds / max(first, 1e-6))))
+    s = time.perf_counter()
+    for _ in range(passes):
+        one_pass()
     dt = time.perf_counter() - s
     nbytes = sum(rows * (K // per_block(t)) * 34 + 2 * M * K + 4 * M * rows for t, K, rows, _, _ in work)
     desc = ", ".join(f"{rows}/{N} rows of the {K}->{N} tensor" for (t, K, rows, _, _), (_, _, N) in zip(work, tensors))
-    return nbytes / dt / 1e9, f"{desc}, M={M}, {dt:.1f} s", threads, dt
+    return (nbytes * passes / dt / 1e9, f"{desc}, M={M}, {passes} passes in {dt:.1f} s on {threads} threads",
+            threads, dt)
 
 
 # ------------------------------------------------------------- distributed ---

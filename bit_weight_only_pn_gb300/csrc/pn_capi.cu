@@ -26,6 +26,23 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return pa < pb + nb && pb < pa + na;
 }
 
+}  // namespace
+
+namespace pn {
+WorkspaceLayout workspace_layout(int num_sms) {
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    WorkspaceLayout L;
+    L.status = 0;
+    L.tagged = 256;
+    L.partials = up(L.tagged + stream_tagged_bytes(num_sms));
+    L.counters = up(L.partials + tc_partial_bytes(num_sms));
+    L.total = up(L.counters + static_cast<size_t>(tc_max_ctas(num_sms) + 1) * sizeof(uint32_t));
+    return L;
+}
+}  // namespace pn
+
+namespace {
+
 // SM count and compute-capability major of the current device (cached).
 pn_status device_info(int* sms, int* major) {
     int dev = 0;
@@ -91,15 +108,18 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
     }
     if (ntc > 0) {
         if (!ws || !aligned(ws, 256)) return PN_EINVAL;
-        int too_small = 0;
+        const pn::WorkspaceLayout L = pn::workspace_layout(sms);
+        if (L.total > ws_bytes) return PN_EINVAL;
+        uint8_t* base = static_cast<uint8_t*>(ws);
+        uint32_t* status = reinterpret_cast<uint32_t*>(base + L.status);
         // one or two tokens: every warp streams its own units; more: thread
         // blocks share each staged activation chunk among eight tiles
         cudaError_t e = M <= 2
-            ? pn::launch_gemv_warp(tc, ntc, M, ws, ws_bytes, sms, g_timeout_ns.load(), g_test_stall.load(), s,
-                                   &too_small)
-            : pn::launch_gemv_tc(tc, ntc, M, ws, ws_bytes, sms, g_timeout_ns.load(), g_test_stall.load(), s,
-                                 &too_small);
-        if (too_small) return PN_EINVAL;
+            ? pn::launch_gemv_stream(tc, ntc, M, status, reinterpret_cast<uint64_t*>(base + L.tagged), sms,
+                                     g_timeout_ns.load(), g_test_stall.load(), s)
+            : pn::launch_gemv_tc(tc, ntc, M, status, reinterpret_cast<float*>(base + L.partials),
+                                 reinterpret_cast<uint32_t*>(base + L.counters), sms, g_timeout_ns.load(),
+                                 g_test_stall.load(), s);
         if (e != cudaSuccess) return PN_ECUDA;
     }
     for (int i = 0; i < nsimt; ++i)
@@ -160,8 +180,7 @@ pn_status pn_unpack(int type, const void* W, int64_t N, int64_t K, float* w, pn_
 size_t pn_workspace_bytes(int64_t total_rows) {
     int sms = 0, major = 0;
     if (total_rows < 0 || device_info(&sms, &major) != PN_OK) return 0;
-    const int64_t tiles = (total_rows + 15) / 16 + pn::kMaxLayer;
-    return pn::workspace_layout(tiles, pn::tc_max_ctas(sms)).total;
+    return pn::workspace_layout(sms).total;
 }
 
 pn_status pn_workspace_init(void* workspace, size_t workspace_bytes, pn_stream stream) {

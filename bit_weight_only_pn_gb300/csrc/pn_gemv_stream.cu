@@ -1,0 +1,863 @@
+// pn_gemv_stream.cu -- PN decode GEMV for one or two tokens on GB300: every
+// warp streams its own share of the weights through a private TMA ring and
+// decodes straight into tensor-core fragments.
+//
+// What is computed: y[m][r] = sum_k d_blk(r,k) * (n(r,k) - z) * x[m][k], the
+// decode GEMV of the tensorless docs ("Why a P100-native weight format": "One
+// lane, one word", "Exact decode in fp32") and its skinny verification batch
+// (v100-skinny README, "How QPN works"), with exact products and fp32 sums.
+//
+// Decode.  A code pair (one code in each 16-bit half of a word, at the same
+// offset, "Codes never straddle the two halves of a word") is masked in place
+// with one AND.  Each half then holds n * 2^off as an fp16 bit pattern with a
+// zero exponent field: the fp16 subnormal n * 2^(off - 24), exactly.  These
+// halves are the A operand of mma.sync m16n8k16 (fp16 in, fp32 accumulate), so
+// the tensor cores form sum_k n_k x_k exactly per product, one accumulator per
+// code offset; the offsets are folded with power-of-two factors afterwards.
+// The zero point comes from the same MMAs: a tile holds 15 weight rows and a
+// 16th row whose codes are all 1, which yields sum_k x_k over exactly the same
+// k-slots, and each weight row's block sum is sum n x - z sum x.
+//
+// Fragment mapping.  An MMA covers 8 blocks (M = 1) or 4 blocks (M = 2): its
+// eight k-pairs are shared out between those blocks and its eight columns are
+// (token, block) pairs, B holding a token's activations only where the k-pair
+// belongs to the column's block.  So every MMA has a full 16 x 16 A tile
+// although M is 1 or 2, and a 16-row x 8-block unit always takes 40 (pn3t) or
+// 32 (pn4t) MMAs.  Each column's sum is scaled by its own block scale d and
+// the columns of one token are then added.
+//
+// Work split.  A unit is a 15-row tile x one 8-block chunk (272 bytes per
+// row).  Units are numbered tile-major over every tensor of the call; the grid
+// splits them into equal contiguous ranges of at least one tile, and the
+// eight warps of a block split the block's range again.  A warp's whole tiles
+// are stored directly; the parts of a tile split between warps are added in
+// warp order by the last warp to deliver (a shared-memory counter); a tile
+// cut by a block boundary is finished by the block holding its first chunks,
+// which picks up the other block's part from 64-bit {tag, value} words.
+// Results do not depend on timing.
+//
+// Every wait is bounded in time; a warp that gives up records PN_ETIMEOUT in
+// the workspace, lets its copies in flight land, and finishes.
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "pn_device.cuh"
+#include "pn_internal.h"
+
+namespace pn {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr int kRows = 15;                                 // weight rows per tile
+constexpr int kChunkBlocks = 8;
+constexpr int kChunkBytes = kChunkBlocks * kBlockBytes;   // 272
+constexpr int kBoxWords = kChunkBytes / 4;                // 68
+constexpr int kBoxBytes = kRows * kChunkBytes;            // 4080
+constexpr int kStageBytes = 4096;
+constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+// The all-ones code rows (pn3t, pn4t) stand in for row 15 of every stage; they
+// sit at the bank offset row 15 would have (15 * 272 = 112 mod 128).
+constexpr int kOnesOffset = kRingBytes + 112;
+constexpr int kOnesBytes = 2 * kChunkBytes + 16;          // + slack for realigning loads
+constexpr int kPartOffset = (kOnesOffset + kOnesBytes + 15) / 16 * 16;
+constexpr int kStreamMaxM = 2;                            // tokens this kernel serves
+constexpr int kSlotFloats = 16 * kStreamMaxM;             // [row][token]
+constexpr int kPartBytes = kWarps * 2 * kSlotFloats * 4;
+constexpr int kCntOffset = kPartOffset + kPartBytes;
+constexpr int kBarOffset = kCntOffset + kWarps * 4;
+constexpr int kSmemBytes = kBarOffset + kWarps * kStages * 8;
+constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
+constexpr uint32_t kStatusTimeout = 5;                    // PN_ETIMEOUT
+constexpr uint32_t kTagFull = 1u;
+
+static_assert(kBoxBytes <= kStageBytes && kStageBytes % 128 == 0, "stages stay TMA-aligned");
+static_assert(kSmemBytes <= 113 * 1024, "two thread blocks fit on one SM");
+static_assert(kBarOffset % 8 == 0, "aligned barriers");
+
+// Zeros read by the lanes whose B fragment is empty (at most 40 code pairs).
+__device__ __align__(16) uint32_t g_zero_pairs[64];
+
+struct STensor {
+    const uint16_t* x;
+    float* y;
+    uint32_t unit_base;     // first unit of this tensor
+    int N;
+    int K;
+    int type;
+    int chunks;             // nb / 8
+    int tiles;              // ceil(N / 15)
+};
+
+struct SParams {
+    CUtensorMap wmap[kMaxLayer];   // PN rows as uint32 [N][row_bytes / 4]; box 68 words x 15 rows
+    STensor t[kMaxLayer];
+    int count;
+    int M;
+    int grid;
+    uint32_t units;                // units * grid < 2^32 (checked on the host)
+    uint32_t* status;
+    uint64_t* tagged;              // [boundary][kSlotFloats] {tag, value bits}
+    uint64_t timeout_ns;
+    int stall_first_step;          // testing aid: see pn_set_test_stall
+};
+
+// Position of a unit: tensor, tile, chunk.
+struct Cursor {
+    int e, tile, chunk;
+    __device__ void locate(const SParams& P, uint32_t u) {
+        e = 0;
+        while (e + 1 < P.count && u >= P.t[e + 1].unit_base) ++e;
+        const uint32_t rel = u - P.t[e].unit_base;
+        const uint32_t ch = static_cast<uint32_t>(P.t[e].chunks);
+        tile = static_cast<int>(rel / ch);
+        chunk = static_cast<int>(rel - static_cast<uint32_t>(tile) * ch);
+    }
+    __device__ void next(const SParams& P) {
+        if (++chunk == P.t[e].chunks) {
+            chunk = 0;
+            if (++tile == P.t[e].tiles) { tile = 0; ++e; }
+        }
+    }
+};
+
+__device__ __forceinline__ uint32_t range_start(const SParams& P, int c) {
+    return P.units * static_cast<uint32_t>(c) / static_cast<uint32_t>(P.grid);
+}
+
+__device__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Lane 0 polls; __syncwarp orders the other lanes' reads of the stage after
+// lane 0's observation of the completed phase.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, int lane) {
+    bool ok = true;
+    if (lane == 0) ok = wait_bounded(bar, parity, limit_ns);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();
+    return ok;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ float half_lo(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+}
+
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulate, accumulator in place.
+__device__ __forceinline__ void mma_acc(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Code pair P of a word, masked in place (see the header): both halves become
+// the fp16 subnormals n * 2^(off - 24).  `sh` is the word shifted right by the
+// format's high shift, which brings the upper pairs into the mantissa field.
+template <int TYPE, int P>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t sh) {
+    using F = Format<TYPE>;
+    constexpr bool kHigh = P >= F::kLowPairs;
+    constexpr int kOff = F::kBits * (kHigh ? P - F::kLowPairs : P);
+    constexpr uint32_t kMask = ((1u << F::kBits) - 1u) << kOff;
+    return (kHigh ? sh : w) & (kMask | (kMask << 16));
+}
+
+// Accumulator class of code pair P: its offset / bits (pn3t 0, 1, 2; pn4t 0, 1).
+template <int TYPE, int P>
+__host__ __device__ constexpr int pair_class() {
+    using F = Format<TYPE>;
+    return P >= F::kLowPairs ? P - F::kLowPairs : P;
+}
+
+template <int TYPE>
+struct Acc {
+    static constexpr int kClasses = TYPE == kPn3t ? 3 : 2;
+    float c[kClasses][4];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int k = 0; k < kClasses; ++k)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[k][i] = 0.0f;
+    }
+    // sum over classes with the classes' power-of-two weights, in units of
+    // 2^-24 (every product carries that factor)
+    __device__ __forceinline__ float fold(int i) const {
+        if constexpr (TYPE == kPn3t) return fmaf(c[2][i], 0.015625f, fmaf(c[1][i], 0.125f, c[0][i]));
+        else return fmaf(c[1][i], 0.0625f, c[0][i]);
+    }
+};
+
+// NP consecutive code-pair activations (fp16 pairs) from p, which is aligned
+// to ALIGN bytes.  Read through the non-coherent path (x is read-only here).
+template <int NP, int ALIGN>
+__device__ __forceinline__ void load_pairs(const uint32_t* p, uint32_t (&v)[NP]) {
+    if constexpr (ALIGN >= 16 && NP % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < NP / 4; ++i) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + i);
+            v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+        }
+    } else if constexpr (ALIGN >= 8 && NP % 2 == 0) {
+#pragma unroll
+        for (int i = 0; i < NP / 2; ++i) {
+            const uint2 q = __ldg(reinterpret_cast<const uint2*>(p) + i);
+            v[2 * i] = q.x; v[2 * i + 1] = q.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) v[i] = __ldg(p + i);
+    }
+}
+
+// Words [w0, w0 + NW) of block b of a staged row (row = 272 bytes), realigned
+// with a per-lane selector: blocks at even positions start 2 bytes into an
+// aligned word (sel 0x5432), odd ones are aligned (sel 0x3210).
+template <int NW>
+__device__ __forceinline__ void load_words_rt(const uint8_t* row, int b, int w0, uint32_t sel, uint32_t (&w)[NW]) {
+    const uint8_t* base = row + ((kBlockBytes * b + 2 + 4 * w0) & ~3);
+    uint32_t v[NW + 1];
+#pragma unroll
+    for (int i = 0; i <= NW; ++i) v[i] = lds_u32(base + 4 * i);
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = prmt(v[i], v[i + 1], sel);
+}
+
+__device__ __forceinline__ float lds_half(const uint8_t* p) { return __half2float(*reinterpret_cast<const __half*>(p)); }
+
+// Per-unit context of a lane.
+struct Lane {
+    int g, t;
+    const uint8_t* r0;     // staged row g
+    const uint8_t* r1;     // staged row g + 8, or the all-ones row for g = 7
+};
+
+// ---------------------------------------------------------------------------
+// One unit (15 rows + ones row, 8 blocks), Mp = 8 / BPM tokens.  Adds the
+// lane's scaled sums to acc: BPM 8 / 4 / 2: acc[h] = row g + 8h of token
+// tok(t); BPM 1: acc[2h + j] = row g + 8h of token 2t + j.
+// xc: the chunk's activations of token 0 (token stride K).
+// ---------------------------------------------------------------------------
+
+template <int TYPE>
+__device__ __forceinline__ void unit_b8(const Lane& L, const uint16_t* xc, int K, int M, float (&acc)[4]) {
+    using F = Format<TYPE>;
+    constexpr int kP = F::kPairs;
+    const int g = L.g, t = L.t;
+    (void)K; (void)M;
+    // k-pair t <-> odd block 2t+1, k-pair t+4 <-> even block 2t; step s of
+    // the unit takes code pair s % kP of word s / kP of both blocks.  The
+    // B columns are the blocks: lane g == 2t+1 carries block 2t+1's
+    // activations in b0, lane g == 2t block 2t's in b1, every other B
+    // register is zero.
+    const uint32_t* xo = (g == 2 * t + 1) ? reinterpret_cast<const uint32_t*>(xc + (2 * t + 1) * F::kPerBlock)
+                                          : g_zero_pairs;
+    const uint32_t* xe = (g == 2 * t) ? reinterpret_cast<const uint32_t*>(xc + 2 * t * F::kPerBlock) : g_zero_pairs;
+    // block 2t starts 4-byte aligned in a staged row: aligned word v[i] at
+    // byte 4i holds (previous half, next half); its words are realigned with
+    // one byte permute, and v[0] / v[8] also hold the two blocks' scales
+    const uint8_t* e0 = L.r0 + 68 * t;
+    const uint8_t* e1 = L.r1 + 68 * t;
+    float d_e0, d_e1;
+    uint32_t we0[8], we1[8], wo0[8], wo1[8];
+    uint32_t v0, v1;
+    {
+        uint32_t a0[9], a1[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+            a0[i] = lds_u32(e0 + 4 * i);
+            a1[i] = lds_u32(e1 + 4 * i);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            we0[i] = prmt(a0[i], a0[i + 1], 0x5432u);
+            we1[i] = prmt(a1[i], a1[i + 1], 0x5432u);
+            wo0[i] = lds_u32(e0 + 36 + 4 * i);
+            wo1[i] = lds_u32(e1 + 36 + 4 * i);
+        }
+        v0 = a0[0];
+        v1 = a1[0];
+        d_e0 = half_lo(v0);
+        d_e1 = half_lo(v1);
+        v0 = a0[8];
+        v1 = a1[8];
+    }
+    Acc<TYPE> A;
+    A.zero();
+    static_for<2 * kP>([&](auto qc) {
+        constexpr int Q = decltype(qc)::value;          // four steps per 16-byte activation load
+        uint32_t bo[4], be[4];
+        load_pairs<4, 16>(xo + 4 * Q, bo);
+        load_pairs<4, 16>(xe + 4 * Q, be);
+        static_for<4>([&](auto jc) {
+            constexpr int S = 4 * Q + decltype(jc)::value;
+            constexpr int W = S / kP, Pp = S % kP;
+            const uint32_t so0 = wo0[W] >> F::kHighShift, so1 = wo1[W] >> F::kHighShift;
+            const uint32_t se0 = we0[W] >> F::kHighShift, se1 = we1[W] >> F::kHighShift;
+            mma_acc(A.c[pair_class<TYPE, Pp>()],
+                    code_pair<TYPE, Pp>(wo0[W], so0), code_pair<TYPE, Pp>(wo1[W], so1),
+                    code_pair<TYPE, Pp>(we0[W], se0), code_pair<TYPE, Pp>(we1[W], se1), bo[S % 4], be[S % 4]);
+        });
+    });
+    const float d_o0 = half_hi(v0), d_o1 = half_hi(v1);        // v[8]: the odd block's scale
+    // column 2t <-> block 2t (even), 2t+1 <-> block 2t+1 (odd); row 15 = sums of x
+    float u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = A.fold(i);
+    const float s_e = __shfl_sync(0xFFFFFFFFu, u[2], 28 + t);
+    const float s_o = __shfl_sync(0xFFFFFFFFu, u[3], 28 + t);
+    constexpr float kNegZ = -static_cast<float>(F::kZero);
+    float r0 = d_e0 * fmaf(s_e, kNegZ, u[0]);
+    r0 = fmaf(d_o0, fmaf(s_o, kNegZ, u[1]), r0);
+    float r1 = d_e1 * fmaf(s_e, kNegZ, u[2]);
+    r1 = fmaf(d_o1, fmaf(s_o, kNegZ, u[3]), r1);
+    r0 += __shfl_xor_sync(0xFFFFFFFFu, r0, 1);
+    r1 += __shfl_xor_sync(0xFFFFFFFFu, r1, 1);
+    r0 += __shfl_xor_sync(0xFFFFFFFFu, r0, 2);
+    r1 += __shfl_xor_sync(0xFFFFFFFFu, r1, 2);
+    acc[0] += r0;
+    acc[1] += r1;
+}
+
+template <int TYPE>
+__device__ __forceinline__ void unit_b4(const Lane& L, const uint16_t* xc, int K, int M, float (&acc)[4]) {
+    using F = Format<TYPE>;
+    constexpr int kP = F::kPairs;
+    constexpr int kSteps = 4 * kP;                 // per group of 4 blocks
+    const int g = L.g, t = L.t;
+    const uint32_t sel = (t & 1) ? 0x3210u : 0x5432u;
+    // column c <-> token c >> 2, block c & 3 of the group; lane t decodes block t
+    const bool has_b = (g & 3) == t && (g >> 2) < M;
+    const uint16_t* xt = xc + static_cast<int64_t>(g >> 2) * K;
+    static_for<2>([&](auto gc) {
+        constexpr int G = decltype(gc)::value;
+        const int blk = 4 * G + t;
+        uint32_t w[2][8];
+        load_words_rt<8>(L.r0, blk, 0, sel, w[0]);
+        load_words_rt<8>(L.r1, blk, 0, sel, w[1]);
+        const uint32_t* xb = has_b ? reinterpret_cast<const uint32_t*>(xt + blk * F::kPerBlock) : g_zero_pairs;
+        uint32_t b0[kSteps], b1[kSteps];
+        load_pairs<kSteps, 16>(xb, b0);                                  // words 0..3
+        load_pairs<kSteps, 16>(has_b ? xb + kSteps : g_zero_pairs, b1);  // words 4..7
+        Acc<TYPE> A;
+        A.zero();
+        static_for<kSteps>([&](auto sc) {
+            constexpr int S = decltype(sc)::value;
+            constexpr int W = S / kP, P = S % kP;
+            const uint32_t s00 = w[0][W] >> F::kHighShift, s10 = w[1][W] >> F::kHighShift;
+            const uint32_t s01 = w[0][W + 4] >> F::kHighShift, s11 = w[1][W + 4] >> F::kHighShift;
+            mma_acc(A.c[pair_class<TYPE, P>()],
+                    code_pair<TYPE, P>(w[0][W], s00), code_pair<TYPE, P>(w[1][W], s10),
+                    code_pair<TYPE, P>(w[0][W + 4], s01), code_pair<TYPE, P>(w[1][W + 4], s11),
+                    b0[S], b1[S]);
+        });
+        float u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) u[i] = A.fold(i);
+        const float s0 = __shfl_sync(0xFFFFFFFFu, u[2], 28 + t);
+        const float s1 = __shfl_sync(0xFFFFFFFFu, u[3], 28 + t);
+        // lane columns 2t, 2t+1 <-> token t >> 1, blocks 4G + 2(t & 1) + {0, 1}
+        const int bb = 4 * G + 2 * (t & 1);
+        constexpr float kNegZ = -static_cast<float>(F::kZero);
+        float v[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint8_t* r = h ? L.r1 : L.r0;
+            const float d0 = lds_half(r + kBlockBytes * bb), d1 = lds_half(r + kBlockBytes * (bb + 1));
+            v[h] = fmaf(d1, fmaf(s1, kNegZ, u[2 * h + 1]), d0 * fmaf(s0, kNegZ, u[2 * h]));
+            v[h] += __shfl_xor_sync(0xFFFFFFFFu, v[h], 1);
+            acc[h] += v[h];
+        }
+    });
+}
+
+template <int BPM, int TYPE>
+__device__ __forceinline__ void unit(const Lane& L, const uint16_t* xc, int K, int M, float (&acc)[4]) {
+    if constexpr (BPM == 8) unit_b8<TYPE>(L, xc, K, M, acc);
+    else unit_b4<TYPE>(L, xc, K, M, acc);
+}
+
+// ------------------------------------------------------------ tile results --
+
+// The (row, token) a lane's acc[i] holds, and whether this lane is the one
+// that stores / deposits it (several lanes hold the same sum for BPM 8 and 4).
+template <int BPM>
+__device__ __forceinline__ bool acc_slot(int g, int t, int i, int& row, int& tok) {
+    row = g + 8 * i;
+    if constexpr (BPM == 8) { tok = 0; return i < 2 && t == 0 && row < kRows; }
+    else { tok = t >> 1; return i < 2 && (t & 1) == 0 && row < kRows; }
+}
+
+// Entries of acc a lane uses: rows g and g + 8.
+template <int BPM>
+__host__ __device__ constexpr int acc_entries() { return 2; }
+
+// Index in a [row][token] slot of the lane's acc[i].
+template <int BPM>
+__device__ __forceinline__ int acc_index(int g, int t, int i) {
+    int row, tok;
+    acc_slot<BPM>(g, t, i, row, tok);
+    return row * kStreamMaxM + tok;
+}
+
+template <int BPM>
+__device__ __forceinline__ void store_tile(const SParams& P, const Cursor& c, int lane, const float (&acc)[4]) {
+    const STensor& T = P.t[c.e];
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int row, tok;
+        if (!acc_slot<BPM>(g, t, i, row, tok)) continue;
+        const int r = c.tile * kRows + row;
+        if (r < T.N && tok < P.M) T.y[static_cast<int64_t>(tok) * T.N + r] = acc[i] * 16777216.0f;   // x 2^24
+    }
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Number of warps of the block with a non-empty share in [wa, wb].
+__device__ __forceinline__ uint32_t contributors(uint32_t n, int wa, int wb) {
+    uint32_t k = 0;
+    for (int w = wa; w <= wb; ++w) k += (n * (w + 1) / kWarps > n * w / kWarps) ? 1u : 0u;
+    return k;
+}
+
+// The warp whose share [n w / 8, n (w + 1) / 8) holds block-relative unit pos.
+__device__ __forceinline__ int warp_of(uint32_t pos, uint32_t n) {
+    int w = static_cast<int>(pos * kWarps / n);
+    while (w > 0 && n * w / kWarps > pos) --w;
+    while (w < kWarps - 1 && n * (w + 1) / kWarps <= pos) ++w;
+    return w;
+}
+
+// Hands this warp's part of a tile split between warps wa..wb to shared
+// memory; the last warp to deliver gets true and the sum in warp order.
+template <int BPM>
+__device__ bool hand_in(uint8_t* smem, int warp, int lane, int wa, int wb, uint32_t n, float (&acc)[4]) {
+    float* parts = reinterpret_cast<float*>(smem + kPartOffset);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + kCntOffset);
+    const int g = lane >> 2, t = lane & 3;
+    float* mine = parts + (warp * 2 + (warp == wa ? 1 : 0)) * kSlotFloats;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int row, tok;
+        if (acc_slot<BPM>(g, t, i, row, tok)) mine[row * kStreamMaxM + tok] = acc[i];
+    }
+    __threadfence_block();
+    __syncwarp();
+    uint32_t old = 0;
+    if (lane == 0) old = atomicAdd(cnt + wa, 1u);
+    old = __shfl_sync(0xFFFFFFFFu, old, 0);
+    if (old + 1 != contributors(n, wa, wb)) return false;
+    __threadfence_block();
+#pragma unroll
+    for (int i = 0; i < acc_entries<BPM>(); ++i) {
+        const int idx = acc_index<BPM>(g, t, i);
+        float s = parts[(wa * 2 + 1) * kSlotFloats + idx];
+        for (int w = wa + 1; w <= wb; ++w)
+            if (n * (w + 1) / kWarps > n * w / kWarps) s += parts[(w * 2) * kSlotFloats + idx];
+        acc[i] = s;
+    }
+    return true;
+}
+
+// This block's part of the tile cut by its left boundary (the tile's later
+// chunks), left for the previous block as {tag, value} words.
+template <int BPM>
+__device__ __forceinline__ void deposit(const SParams& P, int lane, const float (&acc)[4]) {
+    const int g = lane >> 2, t = lane & 3;
+    uint64_t* slot = P.tagged + static_cast<int64_t>(blockIdx.x) * kSlotFloats;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int row, tok;
+        if (acc_slot<BPM>(g, t, i, row, tok) && tok < P.M)
+            st_relaxed_u64(slot + row * kStreamMaxM + tok, (static_cast<uint64_t>(kTagFull) << 32) | __float_as_uint(acc[i]));
+    }
+}
+
+// The tile cut by this block's right boundary: this block holds its first
+// chunks and finishes it once the next block's part has arrived.  poll()
+// checks the words loaded by the previous poll (issued at least one unit of
+// decoding earlier), and loads them again while they are not all tagged, so
+// the wait overlaps the decoding of later units.
+template <int BPM>
+struct Collector {
+    bool pending = false;
+    float acc[4];
+    uint64_t seen[4];
+    uint64_t t0 = 0;
+    Cursor tile{0, 0, 0};
+    __device__ uint64_t* word(const SParams& P, int g, int t, int i) const {
+        return P.tagged + static_cast<int64_t>(blockIdx.x + 1) * kSlotFloats + acc_index<BPM>(g, t, i);
+    }
+    __device__ bool mine(const SParams& P, int g, int t, int i) const {
+        int row, tok;
+        return acc_slot<BPM>(g, t, i, row, tok) && tok < P.M;
+    }
+    __device__ void load(const SParams& P, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int i = 0; i < acc_entries<BPM>(); ++i)
+            seen[i] = mine(P, g, t, i) ? ld_relaxed_u64(word(P, g, t, i)) : (static_cast<uint64_t>(kTagFull) << 32);
+    }
+    __device__ void start(const SParams& P, const Cursor& c, int lane, const float (&v)[4]) {
+        pending = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = v[i];
+        tile = c;
+        load(P, lane);
+        t0 = globaltimer_ns();
+    }
+    __device__ void poll(const SParams& P, int lane) {
+        if (!pending) return;
+        const int g = lane >> 2, t = lane & 3;
+        bool full = true;
+#pragma unroll
+        for (int i = 0; i < acc_entries<BPM>(); ++i) full = full && static_cast<uint32_t>(seen[i] >> 32) == kTagFull;
+        if (__all_sync(0xFFFFFFFFu, full)) {
+#pragma unroll
+            for (int i = 0; i < acc_entries<BPM>(); ++i) {
+                if (!mine(P, g, t, i)) continue;
+                acc[i] += __uint_as_float(static_cast<uint32_t>(seen[i]));    // first chunks + later chunks
+                st_relaxed_u64(word(P, g, t, i), 0ull);
+            }
+            store_tile<BPM>(P, tile, lane, acc);
+            pending = false;
+        } else if (globaltimer_ns() - t0 > P.timeout_ns) {
+            if (lane == 0) atomicCAS(P.status, 0u, kStatusTimeout);
+            pending = false;
+        } else {
+            load(P, lane);
+        }
+    }
+};
+
+// Issue cursor: the next unit to copy, following the block's processing
+// order (see run_warp); the tensor's sizes are kept in registers.
+struct Issuer {
+    uint32_t q;            // sequence position
+    Cursor c;
+    int chunks, tiles;
+    __device__ void set(const SParams& P, uint32_t u) {
+        c.locate(P, u);
+        chunks = P.t[c.e].chunks;
+        tiles = P.t[c.e].tiles;
+    }
+    __device__ void advance(const SParams& P, uint32_t nr, uint32_t c0) {
+        if (++q == nr) { set(P, c0); return; }
+        if (++c.chunk == chunks) {
+            c.chunk = 0;
+            if (++c.tile == tiles) {
+                c.tile = 0;
+                ++c.e;
+                if (c.e < P.count) { chunks = P.t[c.e].chunks; tiles = P.t[c.e].tiles; }
+            }
+        }
+    }
+};
+
+// Ring position of a warp.
+struct Ring {
+    int s = 0;
+    uint32_t phase = 0;
+    uint32_t done = 0, issued = 0;
+};
+
+template <int BPM, int TYPE>
+__device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, Lane& L, const uint16_t* xc, int K,
+                          uint32_t len, uint32_t total, uint32_t nr, uint32_t c0, Ring& R, Issuer& I,
+                          Collector<BPM>& col, float (&acc)[4]) {
+    constexpr int kChunkHalves = kChunkBlocks * Format<TYPE>::kPerBlock;
+    const uint32_t ring = smem_addr(smem) + warp * kStages * kStageBytes;
+    const uint8_t* ring_p = smem + warp * kStages * kStageBytes;
+    const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;
+    const uint8_t* ones = smem + kOnesOffset + (TYPE == kPn3t ? 0 : kChunkBytes);
+    for (uint32_t k = 0; k < len; ++k) {
+        if (!warp_wait(bar0 + 8 * R.s, R.phase, P.timeout_ns, lane)) {
+            if (lane == 0) atomicCAS(P.status, 0u, kStatusTimeout);
+            return false;
+        }
+        const uint8_t* stage = ring_p + R.s * kStageBytes;
+        L.r0 = stage + L.g * kChunkBytes;
+        L.r1 = L.g == 7 ? ones : stage + (L.g + 8) * kChunkBytes;
+        unit<BPM, TYPE>(L, xc, K, P.M, acc);
+        xc += kChunkHalves;
+        __syncwarp();
+        ++R.done;
+        if (R.issued < total) {                   // refill this stage
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                const uint32_t bar = bar0 + 8 * R.s;
+                mbar_arrive_expect_tx(bar, kBoxBytes);
+                tma_load_2d(ring + R.s * kStageBytes, &P.wmap[I.c.e], I.c.chunk * kBoxWords, I.c.tile * kRows, bar);
+            }
+            I.advance(P, nr, c0);
+            ++R.issued;
+        }
+        if (++R.s == kStages) { R.s = 0; R.phase ^= 1u; }
+        col.poll(P, lane);
+    }
+    return true;
+}
+
+// A block's units are processed in this order: first its part of the tile
+// that continues into the next block (nr units, the last of its range), then
+// the rest of its range in order.  Its part of the tile begun by the previous
+// block comes right after, so both tiles that cross a block boundary are
+// settled early; the next block's part of the first one is collected while
+// later units decode.  The eight warps split this sequence into equal
+// contiguous shares.
+template <int BPM>
+__device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, uint32_t c0, uint32_t c1) {
+    const uint32_t n = c1 - c0;
+    Cursor lastc{0, 0, 0};
+    lastc.locate(P, c1 - 1);
+    const uint32_t nr = lastc.chunk != P.t[lastc.e].chunks - 1 ? static_cast<uint32_t>(lastc.chunk + 1) : 0u;
+    const uint32_t p0 = n * static_cast<uint32_t>(warp) / kWarps;
+    const uint32_t p1 = n * static_cast<uint32_t>(warp + 1) / kWarps;
+    auto seq_unit = [&](uint32_t q) { return q < nr ? c1 - nr + q : c0 + (q - nr); };
+    const uint32_t total = p1 - p0;
+    const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;
+    const uint32_t ring = smem_addr(smem) + warp * kStages * kStageBytes;
+
+    Issuer I;
+    I.q = p0;
+    if (total > 0) I.set(P, seq_unit(p0));
+    if (lane == 0 && total > 0) {
+        // warm L2 with this warp's first units while the previous kernel finishes
+        Issuer J = I;
+        for (uint32_t k = 0; k < kStages && k < total; ++k) {
+            tma_prefetch_l2_2d(&P.wmap[J.c.e], J.c.chunk * kBoxWords, J.c.tile * kRows);
+            J.advance(P, nr, c0);
+        }
+    }
+    griddep_wait();
+    __syncwarp();
+    if (total == 0) return;
+
+    Ring R;
+    for (int s = 0; s < kStages && R.issued < total; ++s) {
+        if (lane == 0) {
+            const uint32_t bar = bar0 + 8 * s;
+            mbar_arrive_expect_tx(bar, kBoxBytes);
+            // (testing aid: with stall_first_step a warp's first unit is
+            // announced but never copied, so its wait can only time out)
+            if (!(s == 0 && P.stall_first_step))
+                tma_load_2d(ring + s * kStageBytes, &P.wmap[I.c.e], I.c.chunk * kBoxWords, I.c.tile * kRows, bar);
+        }
+        I.advance(P, nr, c0);
+        ++R.issued;
+    }
+
+    Lane L;
+    L.g = lane >> 2;
+    L.t = lane & 3;
+    Collector<BPM> col;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    uint32_t q = p0;
+    Cursor cur{0, 0, 0};
+    cur.locate(P, seq_unit(q));
+    bool ok = true;
+    while (q < p1) {
+        const STensor& T = P.t[cur.e];
+        const uint32_t run_end = q < nr ? (nr < p1 ? nr : p1) : p1;
+        const uint32_t room = static_cast<uint32_t>(T.chunks - cur.chunk);
+        const uint32_t len = run_end - q < room ? run_end - q : room;
+        const uint16_t* xc = T.x + cur.chunk * kChunkBlocks * per_block(T.type);
+        ok = T.type == kPn3t ? part_loop<BPM, kPn3t>(P, smem, warp, lane, L, xc, T.K, len, total, nr, c0, R, I, col, acc)
+                             : part_loop<BPM, kPn4t>(P, smem, warp, lane, L, xc, T.K, len, total, nr, c0, R, I, col, acc);
+        if (!ok) break;
+        // this warp's part of tile cur.tile ends here
+        const uint32_t tbeg = T.unit_base + static_cast<uint32_t>(cur.tile) * T.chunks;
+        const uint32_t tend = tbeg + T.chunks;
+        const bool right_cut = tend > c1, left_cut = tbeg < c0;
+        const uint32_t ss = right_cut ? 0u : nr + (left_cut ? 0u : tbeg - c0);   // the tile's sequence range
+        const uint32_t se = right_cut ? nr : nr + (tend - c0);
+        const int wa = warp_of(ss, n), wb = warp_of(se - 1, n);
+        if (wa == wb || hand_in<BPM>(smem, warp, lane, wa, wb, n, acc)) {
+            if (right_cut) col.start(P, cur, lane, acc);
+            else if (left_cut) deposit<BPM>(P, lane, acc);
+            else store_tile<BPM>(P, cur, lane, acc);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = 0.0f;
+        q += len;
+        if (q == nr && q < p1) {
+            cur.locate(P, c0);
+        } else {
+            cur.chunk += static_cast<int>(len);
+            if (cur.chunk == T.chunks) {
+                cur.chunk = 0;
+                if (++cur.tile == T.tiles) { cur.tile = 0; ++cur.e; }
+            }
+        }
+    }
+    if (!ok) {
+        if (lane == 0) {
+            // after a timeout: let every copy this warp started land before the block can exit
+            for (uint32_t k = R.done; k < R.issued; ++k) {
+                if (k == 0 && P.stall_first_step) continue;   // never copied
+                wait_bounded(bar0 + 8 * (k % kStages), (k / kStages) & 1u, kDrainLimitNs);
+            }
+        }
+        __syncwarp();
+        return;
+    }
+    while (col.pending) {
+        __nanosleep(64);
+        col.poll(P, lane);
+    }
+}
+
+template <int BPM>
+__global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const __grid_constant__ SParams P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    griddep_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t c0 = range_start(P, blockIdx.x), c1 = range_start(P, blockIdx.x + 1);
+    // all-ones code rows: pn3t (codes 1 at 0, 3, 6, 9, 12 of each half), pn4t
+    // (1 in every nibble); scales 0
+    for (int i = threadIdx.x; i < kOnesBytes / 2; i += kThreads) {
+        uint16_t v = 0;
+        if (i < 2 * (kChunkBytes / 2)) {
+            const int row = i / (kChunkBytes / 2), hw = i % (kChunkBytes / 2);   // half-word in the row
+            const int inblk = hw % (kBlockBytes / 2);
+            if (inblk != 0) v = row == 0 ? 0x1249u : 0x1111u;
+        }
+        reinterpret_cast<uint16_t*>(smem + kOnesOffset)[i] = v;
+    }
+    if (lane == 0) {
+        const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;
+        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+        reinterpret_cast<uint32_t*>(smem + kCntOffset)[warp] = 0u;
+    }
+    __syncthreads();
+    run_warp<BPM>(P, smem, warp, lane, c0, c1);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Tensor map over a tensor's PN rows viewed as uint32 [N][row_bytes / 4],
+// box = one 8-block chunk (68 words) x 15 rows; rows past N read as zero.
+bool encode_rows(CUtensorMap* map, const GemvTensor& t) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(t.nb) * kBlockBytes;
+    const cuuint64_t dims[2] = {row_bytes / 4, static_cast<cuuint64_t>(t.N)};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxWords), static_cast<cuuint32_t>(kRows)};
+    const cuuint32_t estride[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(t.W), dims, strides, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BPM>
+cudaError_t launch_bpm(const SParams& P, cudaStream_t s) {
+    static bool attr_set = false;   // per process; the attribute is per function
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BPM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(P.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BPM>, P);
+}
+
+}  // namespace
+
+int stream_max_ctas(int num_sms) { return 2 * num_sms; }
+
+size_t stream_tagged_bytes(int num_sms) {
+    return static_cast<size_t>(stream_max_ctas(num_sms) + 1) * kSlotFloats * sizeof(uint64_t);
+}
+
+cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* status, uint64_t* tagged,
+                               int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s) {
+    if (M < 1 || M > kStreamMaxM || count < 1 || count > kMaxLayer) return cudaErrorInvalidValue;
+    SParams P{};
+    uint64_t units = 0;
+    int max_chunks = 1;
+    for (int e = 0; e < count; ++e) {
+        STensor& T = P.t[e];
+        T.x = t[e].x;
+        T.y = t[e].y;
+        T.N = t[e].N;
+        T.type = t[e].type;
+        T.K = t[e].nb * per_block(t[e].type);
+        T.chunks = t[e].nb / kChunkBlocks;
+        T.tiles = (t[e].N + kRows - 1) / kRows;
+        T.unit_base = static_cast<uint32_t>(units);
+        if (!encode_rows(&P.wmap[e], t[e])) return cudaErrorInvalidValue;
+        units += static_cast<uint64_t>(T.chunks) * T.tiles;
+        max_chunks = T.chunks > max_chunks ? T.chunks : max_chunks;
+    }
+    P.count = count;
+    P.M = M;
+    // every block range spans at least one whole tile, so a tile has at most two blocks
+    uint64_t grid = units / static_cast<uint64_t>(max_chunks);
+    if (grid > static_cast<uint64_t>(stream_max_ctas(num_sms))) grid = stream_max_ctas(num_sms);
+    if (grid < 1) grid = 1;
+    if (units * grid >= (1ull << 32) || units * kWarps >= (1ull << 32)) return cudaErrorInvalidValue;
+    P.grid = static_cast<int>(grid);
+    P.units = static_cast<uint32_t>(units);
+    P.status = status;
+    P.tagged = tagged;
+    P.timeout_ns = timeout_ns;
+    P.stall_first_step = stall;
+    return M == 1 ? launch_bpm<8>(P, s) : launch_bpm<4>(P, s);
+}
+
+}  // namespace pn

@@ -731,25 +731,14 @@ bool encode_x(CUtensorMap* map, const GemvTensor& t, int M) {
 
 }  // namespace
 
-// Workspace: status word, then for every thread-block boundary (one more
-// than the largest grid) two partial-sum slots and a counter (batch kernel)
-// and one row of tagged words (warp kernel).
-WorkspaceLayout workspace_layout(int64_t /*total_tiles*/, int max_ctas) {
-    WorkspaceLayout L;
-    L.status = 0;
-    L.partials = 256;
-    const size_t boundaries = static_cast<size_t>(max_ctas) + 1;
-    L.counters = L.partials + boundaries * 2 * kSlotFloats * sizeof(float);
-    L.tagged = L.counters + ((boundaries * 4 + 255) / 256) * 256;
-    L.total = L.tagged + boundaries * kTileRows * 2 * sizeof(uint64_t);
-    return L;
+int tc_max_ctas(int num_sms) { return num_sms; }
+
+size_t tc_partial_bytes(int num_sms) {
+    return static_cast<size_t>(tc_max_ctas(num_sms) + 1) * 2 * kSlotFloats * sizeof(float);
 }
 
-int tc_max_ctas(int num_sms) { return warp_max_ctas(num_sms); }
-
-cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, void* workspace,
-                           size_t workspace_bytes, int num_sms, uint64_t timeout_ns, int stall,
-                           cudaStream_t s, int* needs_bytes_out) {
+cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* status, float* partials,
+                           uint32_t* counters, int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s) {
     TcParams P{};
     uint64_t units = 0;
     int max_chunks = 1;
@@ -770,21 +759,14 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, void* workspac
     P.M = M;
     // every range spans at least one whole tile, so a tile has at most two owners
     uint64_t grid = units / static_cast<uint64_t>(max_chunks);
-    if (grid > static_cast<uint64_t>(num_sms)) grid = num_sms;
+    if (grid > static_cast<uint64_t>(tc_max_ctas(num_sms))) grid = tc_max_ctas(num_sms);
     if (grid < 1) grid = 1;
     if (units * grid >= (1ull << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
     P.grid = static_cast<int>(grid);
     P.units = static_cast<uint32_t>(units);
-    const WorkspaceLayout L = workspace_layout(0, tc_max_ctas(num_sms));
-    if (needs_bytes_out) *needs_bytes_out = 0;
-    if (L.total > workspace_bytes) {
-        if (needs_bytes_out) *needs_bytes_out = 1;
-        return cudaSuccess;
-    }
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    P.status = reinterpret_cast<uint32_t*>(ws + L.status);
-    P.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
-    P.partials = reinterpret_cast<float*>(ws + L.partials);
+    P.status = status;
+    P.counters = counters;
+    P.partials = partials;
     P.timeout_ns = timeout_ns;
     P.stall_first_step = stall;
 

@@ -25,31 +25,35 @@ cudaError_t launch_pack(int type, const float* w, int64_t N, int64_t nb, void* W
 // CUDA-core GEMV: any nb, W and x 2-byte aligned, y 4-byte aligned.
 cudaError_t launch_gemv_simt(const GemvTensor& t, int M, cudaStream_t s);
 
-// Workspace layout of the tensor-core GEMV (all offsets in bytes).
+// Workspace of the tensor-core GEMVs (offsets in bytes), every completed call
+// leaves it zeroed:
+//   status    uint32 status word (padded to 256 bytes);
+//   tagged    one-/two-token kernel: per thread-block boundary, one
+//             [16 rows][2 tokens] slot of 64-bit {tag, value} words through
+//             which a block hands its part of a shared tile to its neighbour;
+//   partials  batch kernel: per boundary, two [16 rows][8 tokens] fp32 slots;
+//   counters  batch kernel: one uint32 per boundary.
 struct WorkspaceLayout {
-    size_t status = 0;        // uint32 status word (+ padding to 256)
-    size_t partials = 256;    // float slots [boundary][side][16 rows x 8 tokens] (batch kernel)
-    size_t counters = 0;      // uint32 per thread-block boundary (batch kernel)
-    size_t tagged = 0;        // 64-bit {value, tag} words [boundary][16 rows x 2 tokens] (warp kernel)
+    size_t status = 0;
+    size_t tagged = 0;
+    size_t partials = 0;
+    size_t counters = 0;
     size_t total = 0;
 };
-WorkspaceLayout workspace_layout(int64_t total_tiles, int max_ctas);
+WorkspaceLayout workspace_layout(int num_sms);
 
-// Tensor-core GEMV over `count` tensors (every one with nb % 8 == 0 and W, x
-// 16-byte aligned).  `workspace` has the layout above, zeroed.
-cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, void* workspace,
-                           size_t workspace_bytes, int num_sms, uint64_t timeout_ns, int stall,
-                           cudaStream_t s, int* needs_bytes_out);
+// Tensor-core GEMV for M <= 2 over `count` tensors (every one with nb % 8 == 0
+// and W, x 16-byte aligned): every warp streams its own units.
+cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* status, uint64_t* tagged,
+                               int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s);
+int stream_max_ctas(int num_sms);
+size_t stream_tagged_bytes(int num_sms);
 
-// Most thread blocks any tensor-core GEMV launch uses; the workspace holds a
-// boundary slot pair for each.
+// Tensor-core GEMV for 3 <= M <= 8 (same eligibility): thread blocks share
+// each staged activation chunk among eight tiles.
+cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* status, float* partials,
+                           uint32_t* counters, int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s);
 int tc_max_ctas(int num_sms);
-
-// Tensor-core GEMV for M <= 2 in which every warp streams its own units
-// (same eligibility, same workspace layout as launch_gemv_tc).
-cudaError_t launch_gemv_warp(const GemvTensor* t, int count, int M, void* workspace,
-                             size_t workspace_bytes, int num_sms, uint64_t timeout_ns, int stall,
-                             cudaStream_t s, int* needs_bytes_out);
-int warp_max_ctas(int num_sms);
+size_t tc_partial_bytes(int num_sms);
 
 }  // namespace pn

@@ -26,9 +26,8 @@
 
 namespace {
 
-// Room for the workspace of a device with up to 203 SMs: the workspace size
-// depends only on the SM count s: 256 + 1280 * (2s + 1) bytes plus the
-// (2s + 1) counters rounded up to 256 bytes.
+// Room for the workspace of a device with up to 339 SMs (the workspace size
+// depends only on the SM count: about 1.5 KiB per SM).
 constexpr size_t kNoAllocScratchBytes = 512 * 1024;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -67,9 +66,10 @@ extern "C" pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t
     void* ws = nullptr;
     pn_status st = scratch_address(&ws);
     if (st != PN_OK) return st;
-    // The array keeps the last call's contents.  The status word and the
-    // boundary counters must start at zero; a completed call leaves them zero,
-    // an aborted one may not, so both are cleared before every launch.
+    // The array keeps the last call's contents.  The status word, the tagged
+    // hand-off words and the counters must start at zero; a completed call
+    // leaves them zero, an aborted one may not, so the whole workspace is
+    // cleared before every launch.
     int sms = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -77,11 +77,8 @@ extern "C" pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t
         cudaGetLastError();
         return PN_ECUDA;
     }
-    const pn::WorkspaceLayout L = pn::workspace_layout(0, pn::tc_max_ctas(sms));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    unsigned char* base = static_cast<unsigned char*>(ws);
-    if (cudaMemsetAsync(base + L.status, 0, L.partials - L.status, s) != cudaSuccess ||
-        cudaMemsetAsync(base + L.counters, 0, L.total - L.counters, s) != cudaSuccess) {
+    const pn::WorkspaceLayout L = pn::workspace_layout(sms);
+    if (cudaMemsetAsync(ws, 0, L.total, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return PN_ECUDA;
     }

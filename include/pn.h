@@ -109,11 +109,14 @@ pn_status pn_pack(int type, const float* w, int64_t N, int64_t K, void* W, pn_st
 pn_status pn_unpack(int type, const void* W, int64_t N, int64_t K, float* w, pn_stream stream);
 
 /*
- * Workspace for the GEMV calls.  The tensor-core kernel splits rows and K
- * blocks evenly over the SMs; a tile whose K range is split between thread
- * blocks is summed by the last contributor in a fixed order, so results are
- * deterministic.  That needs device scratch: a status word, one counter per
- * 16-row tile, and two partial-sum slots per thread block.
+ * Workspace for the GEMV calls.  The tensor-core kernels split the rows and K
+ * blocks of all tensors of a call evenly over their thread blocks; a tile of
+ * rows whose K range is split between two thread blocks is finished by one of
+ * them, which adds the other block's part in a fixed order, so results are
+ * deterministic.  That needs device scratch: a status word and, per
+ * thread-block boundary, hand-off slots and a counter.  The size depends only
+ * on the device's SM count (about 1.5 KiB per SM), so calls of any shape can
+ * share one workspace.
  *
  * pn_workspace_bytes(total_rows): bytes needed by one call whose tensors have
  * total_rows rows in all (sum of N), on the current device.
@@ -178,7 +181,7 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
  *
  * Scratch: a fixed 512 KiB array in the library's device image, which every
  * GPU that loads the library holds until the process exits.  A device whose
- * workspace (pn_workspace_bytes) would not fit (more than 203 SMs) gets
+ * workspace (pn_workspace_bytes) would not fit (more than 339 SMs) gets
  * PN_EINVAL and nothing is launched.  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress, which may load the
  * library's device module); make that first call before capturing a stream
