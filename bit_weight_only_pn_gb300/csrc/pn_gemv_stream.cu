@@ -31,10 +31,10 @@
 // splits them into equal contiguous ranges of at least one tile, and the
 // eight warps of a block split the block's range again.  A warp's whole tiles
 // are stored directly; the parts of a tile split between warps are added in
-// warp order by the last warp to deliver (a shared-memory counter); a tile
-// cut by a block boundary is finished by the block holding its first chunks,
-// which picks up the other block's part from 64-bit {tag, value} words.
-// Results do not depend on timing.
+// warp order by the last warp to deliver (a shared-memory counter); for a tile
+// cut by a block boundary both blocks swap their tagged part into a shared
+// slot with a 64-bit atomic exchange and the block that gets the other's part
+// back adds first chunks + later chunks.  Results do not depend on timing.
 //
 // Every wait is bounded in time; a warp that gives up records PN_ETIMEOUT in
 // the workspace, lets its copies in flight land, and finishes.
@@ -73,7 +73,6 @@ constexpr int kBarOffset = kCntOffset + kWarps * 4;
 constexpr int kSmemBytes = kBarOffset + kWarps * kStages * 8;
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                    // PN_ETIMEOUT
-constexpr uint32_t kTagFull = 1u;
 
 static_assert(kBoxBytes <= kStageBytes && kStageBytes % 128 == 0, "stages stay TMA-aligned");
 static_assert(kSmemBytes <= 113 * 1024, "two thread blocks fit on one SM");
@@ -116,12 +115,6 @@ struct Cursor {
         const uint32_t ch = static_cast<uint32_t>(P.t[e].chunks);
         tile = static_cast<int>(rel / ch);
         chunk = static_cast<int>(rel - static_cast<uint32_t>(tile) * ch);
-    }
-    __device__ void next(const SParams& P) {
-        if (++chunk == P.t[e].chunks) {
-            chunk = 0;
-            if (++tile == P.t[e].tiles) { tile = 0; ++e; }
-        }
     }
 };
 
@@ -435,11 +428,6 @@ __device__ __forceinline__ void store_tile(const SParams& P, const Cursor& c, in
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
 
 // Number of warps of the block with a non-empty share in [wa, wb].
 __device__ __forceinline__ uint32_t contributors(uint32_t n, int wa, int wb) {
@@ -487,76 +475,39 @@ __device__ bool hand_in(uint8_t* smem, int warp, int lane, int wa, int wb, uint3
     return true;
 }
 
-// This block's part of the tile cut by its left boundary (the tile's later
-// chunks), left for the previous block as {tag, value} words.
-template <int BPM>
-__device__ __forceinline__ void deposit(const SParams& P, int lane, const float (&acc)[4]) {
-    const int g = lane >> 2, t = lane & 3;
-    uint64_t* slot = P.tagged + static_cast<int64_t>(blockIdx.x) * kSlotFloats;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int row, tok;
-        if (acc_slot<BPM>(g, t, i, row, tok) && tok < P.M)
-            st_relaxed_u64(slot + row * kStreamMaxM + tok, (static_cast<uint64_t>(kTagFull) << 32) | __float_as_uint(acc[i]));
-    }
+__device__ __forceinline__ uint64_t atom_exch_u64(uint64_t* p, uint64_t v) {
+    return atomicExch(reinterpret_cast<unsigned long long*>(p), static_cast<unsigned long long>(v));
 }
 
-// The tile cut by this block's right boundary: this block holds its first
-// chunks and finishes it once the next block's part has arrived.  poll()
-// checks the words loaded by the previous poll (issued at least one unit of
-// decoding earlier), and loads them again while they are not all tagged, so
-// the wait overlaps the decoding of later units.
+// A tile cut by a thread-block boundary has two parts, the first chunks
+// (held by the block before the boundary) and the rest (held by the block
+// after it).  Each side swaps its part, tagged with which part it is, into
+// the boundary's slot with one 64-bit atomic exchange per output; exactly one
+// side gets the other's part back, adds first + second in that order, stores
+// the output and clears the slot.  Neither side waits for the other.
+constexpr uint32_t kTagFirst = 1u, kTagSecond = 2u;
+
 template <int BPM>
-struct Collector {
-    bool pending = false;
-    float acc[4];
-    uint64_t seen[4];
-    uint64_t t0 = 0;
-    Cursor tile{0, 0, 0};
-    __device__ uint64_t* word(const SParams& P, int g, int t, int i) const {
-        return P.tagged + static_cast<int64_t>(blockIdx.x + 1) * kSlotFloats + acc_index<BPM>(g, t, i);
-    }
-    __device__ bool mine(const SParams& P, int g, int t, int i) const {
+__device__ __forceinline__ void exchange(const SParams& P, const Cursor& c, int lane, bool first, int boundary,
+                                         const float (&acc)[4]) {
+    const int g = lane >> 2, t = lane & 3;
+    uint64_t* slot = P.tagged + static_cast<int64_t>(boundary) * kSlotFloats;
+    const uint64_t tag = static_cast<uint64_t>(first ? kTagFirst : kTagSecond) << 32;
+    const STensor& T = P.t[c.e];
+#pragma unroll
+    for (int i = 0; i < acc_entries<BPM>(); ++i) {
         int row, tok;
-        return acc_slot<BPM>(g, t, i, row, tok) && tok < P.M;
+        if (!(acc_slot<BPM>(g, t, i, row, tok) && tok < P.M)) continue;
+        uint64_t* w = slot + acc_index<BPM>(g, t, i);
+        const uint64_t got = atom_exch_u64(w, tag | __float_as_uint(acc[i]));
+        if ((got >> 32) == 0) continue;                       // the other side finishes this output
+        const float other = __uint_as_float(static_cast<uint32_t>(got));
+        const float v = first ? acc[i] + other : other + acc[i];     // first chunks + later chunks
+        const int r = c.tile * kRows + row;
+        if (r < T.N) T.y[static_cast<int64_t>(tok) * T.N + r] = v * 16777216.0f;    // x 2^24
+        st_relaxed_u64(w, 0ull);
     }
-    __device__ void load(const SParams& P, int lane) {
-        const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-        for (int i = 0; i < acc_entries<BPM>(); ++i)
-            seen[i] = mine(P, g, t, i) ? ld_relaxed_u64(word(P, g, t, i)) : (static_cast<uint64_t>(kTagFull) << 32);
-    }
-    __device__ void start(const SParams& P, const Cursor& c, int lane, const float (&v)[4]) {
-        pending = true;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = v[i];
-        tile = c;
-        load(P, lane);
-        t0 = globaltimer_ns();
-    }
-    __device__ void poll(const SParams& P, int lane) {
-        if (!pending) return;
-        const int g = lane >> 2, t = lane & 3;
-        bool full = true;
-#pragma unroll
-        for (int i = 0; i < acc_entries<BPM>(); ++i) full = full && static_cast<uint32_t>(seen[i] >> 32) == kTagFull;
-        if (__all_sync(0xFFFFFFFFu, full)) {
-#pragma unroll
-            for (int i = 0; i < acc_entries<BPM>(); ++i) {
-                if (!mine(P, g, t, i)) continue;
-                acc[i] += __uint_as_float(static_cast<uint32_t>(seen[i]));    // first chunks + later chunks
-                st_relaxed_u64(word(P, g, t, i), 0ull);
-            }
-            store_tile<BPM>(P, tile, lane, acc);
-            pending = false;
-        } else if (globaltimer_ns() - t0 > P.timeout_ns) {
-            if (lane == 0) atomicCAS(P.status, 0u, kStatusTimeout);
-            pending = false;
-        } else {
-            load(P, lane);
-        }
-    }
-};
+}
 
 // Issue cursor: the next unit to copy, following the block's processing
 // order (see run_warp); the tensor's sizes are kept in registers.
@@ -592,7 +543,7 @@ struct Ring {
 template <int BPM, int TYPE>
 __device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, Lane& L, const uint16_t* xc, int K,
                           uint32_t len, uint32_t total, uint32_t nr, uint32_t c0, Ring& R, Issuer& I,
-                          Collector<BPM>& col, float (&acc)[4]) {
+                          float (&acc)[4]) {
     constexpr int kChunkHalves = kChunkBlocks * Format<TYPE>::kPerBlock;
     const uint32_t ring = smem_addr(smem) + warp * kStages * kStageBytes;
     const uint8_t* ring_p = smem + warp * kStages * kStageBytes;
@@ -621,7 +572,6 @@ __device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, L
             ++R.issued;
         }
         if (++R.s == kStages) { R.s = 0; R.phase ^= 1u; }
-        col.poll(P, lane);
     }
     return true;
 }
@@ -630,9 +580,8 @@ __device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, L
 // that continues into the next block (nr units, the last of its range), then
 // the rest of its range in order.  Its part of the tile begun by the previous
 // block comes right after, so both tiles that cross a block boundary are
-// settled early; the next block's part of the first one is collected while
-// later units decode.  The eight warps split this sequence into equal
-// contiguous shares.
+// exchanged early, away from the kernel's tail.  The eight warps split this
+// sequence into equal contiguous shares.
 template <int BPM>
 __device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, uint32_t c0, uint32_t c1) {
     const uint32_t n = c1 - c0;
@@ -678,7 +627,6 @@ __device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, ui
     Lane L;
     L.g = lane >> 2;
     L.t = lane & 3;
-    Collector<BPM> col;
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     uint32_t q = p0;
     Cursor cur{0, 0, 0};
@@ -690,8 +638,8 @@ __device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, ui
         const uint32_t room = static_cast<uint32_t>(T.chunks - cur.chunk);
         const uint32_t len = run_end - q < room ? run_end - q : room;
         const uint16_t* xc = T.x + cur.chunk * kChunkBlocks * per_block(T.type);
-        ok = T.type == kPn3t ? part_loop<BPM, kPn3t>(P, smem, warp, lane, L, xc, T.K, len, total, nr, c0, R, I, col, acc)
-                             : part_loop<BPM, kPn4t>(P, smem, warp, lane, L, xc, T.K, len, total, nr, c0, R, I, col, acc);
+        ok = T.type == kPn3t ? part_loop<BPM, kPn3t>(P, smem, warp, lane, L, xc, T.K, len, total, nr, c0, R, I, acc)
+                             : part_loop<BPM, kPn4t>(P, smem, warp, lane, L, xc, T.K, len, total, nr, c0, R, I, acc);
         if (!ok) break;
         // this warp's part of tile cur.tile ends here
         const uint32_t tbeg = T.unit_base + static_cast<uint32_t>(cur.tile) * T.chunks;
@@ -701,9 +649,11 @@ __device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, ui
         const uint32_t se = right_cut ? nr : nr + (tend - c0);
         const int wa = warp_of(ss, n), wb = warp_of(se - 1, n);
         if (wa == wb || hand_in<BPM>(smem, warp, lane, wa, wb, n, acc)) {
-            if (right_cut) col.start(P, cur, lane, acc);
-            else if (left_cut) deposit<BPM>(P, lane, acc);
-            else store_tile<BPM>(P, cur, lane, acc);
+            if (right_cut || left_cut) {
+                exchange<BPM>(P, cur, lane, right_cut, right_cut ? blockIdx.x + 1 : blockIdx.x, acc);
+            } else {
+                store_tile<BPM>(P, cur, lane, acc);
+            }
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[i] = 0.0f;
@@ -728,10 +678,6 @@ __device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, ui
         }
         __syncwarp();
         return;
-    }
-    while (col.pending) {
-        __nanosleep(64);
-        col.poll(P, lane);
     }
 }
 
