@@ -171,15 +171,13 @@ __device__ __forceinline__ uint32_t realign16(uint32_t a, uint32_t b) {
     return __byte_perm(a, b, 0x5432);
 }
 
-// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1, const float (&c)[4]) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1),
-          "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+// C += A * B, m16n8k16, fp16 inputs, fp32 accumulate, accumulator in place.
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t h) {
@@ -218,10 +216,12 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t word, uint32_t shifted)
 //
 // A staged tile holds 16 rows of one 8-block chunk, 272 bytes apart.  Lane
 // (g, t) of a warp (g = lane / 4, t = lane % 4) owns MMA rows g and g + 8 and
-// code words 2t, 2t + 1 of every block; code pair P of word 2t gives the A
-// register for k = 2t, 2t + 1 and the same pair of word 2t + 1 the one for
-// k = 2t + 8, 2t + 9 of the block's P-th m16n8k16 product, so a block is
-// kPairs products whose 16 k-slots all lie in the block (one scale each).
+// code words 2t, 2t + 1 of every block: ten (pn3t) or eight (pn4t) code pairs
+// q = 0, 1, ... (word 2t's pairs first), whose activations are the lane's
+// consecutive x pairs 2 * kPerWord * t / 2 + q.  The block's s-th m16n8k16
+// product takes pairs q = 2s (k-slots 2t, 2t+1) and q = 2s + 1 (k-slots
+// 2t + 8, 2t + 9) of every lane, so its B fragment is two adjacent x pairs,
+// one 64-bit load, and its 16 k-slots all lie in the block (one scale).
 
 constexpr int kStagedRowBytes = 8 * kBlockBytes;    // 272: rows of a staged tile
 
@@ -271,9 +271,17 @@ __device__ __forceinline__ void load_words(const uint8_t* row, int t, uint32_t& 
     }
 }
 
-// Block B of staged rows r0 (MMA row g) and r1 (row g + 8) times the x pairs
-// xb (xb[P]: word 2t, pair P; xb[kPairs + P]: word 2t + 1, pair P).  The
-// block's products start from zero and are scaled by the rows' d in fp32:
+// Code pair q of the lane's two words (q < kPairs: word 2t, else word 2t+1).
+template <int TYPE, int Q>
+__device__ __forceinline__ uint32_t lane_pair(uint32_t w0, uint32_t s0, uint32_t w1, uint32_t s1) {
+    constexpr int kP = Format<TYPE>::kPairs;
+    if constexpr (Q < kP) return decode_pair<TYPE, Q>(w0, s0);
+    else return decode_pair<TYPE, Q - kP>(w1, s1);
+}
+
+// Block B of staged rows r0 (MMA row g) and r1 (row g + 8) times the lane's x
+// pairs xb (xb[q] pairs with code pair q, see above).  The block's products
+// start from zero and are scaled by the rows' d in fp32:
 // part[0..1] += d(r0) * (columns 2t, 2t+1), part[2..3] += d(r1) * (same).
 // With kOddCols false the odd columns (part[1], part[3]) are left alone, for
 // callers that only read even columns (a single token).
@@ -289,14 +297,14 @@ __device__ __forceinline__ void block_mma(const uint8_t* r0, const uint8_t* r1, 
     const uint32_t s00 = w00 >> F::kHighShift, s10 = w10 >> F::kHighShift;
     const uint32_t s01 = w01 >> F::kHighShift, s11 = w11 >> F::kHighShift;
     float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    static_for<F::kPairs>([&](auto pc) {
-        constexpr int P = decltype(pc)::value;
-        const uint32_t a[4] = {
-            decode_pair<TYPE, P>(w00, s00),   // row g,   k = 2t, 2t+1   <- word 2t
-            decode_pair<TYPE, P>(w01, s01),   // row g+8, k = 2t, 2t+1   <- word 2t
-            decode_pair<TYPE, P>(w10, s10),   // row g,   k = 2t+8, 2t+9 <- word 2t+1
-            decode_pair<TYPE, P>(w11, s11)};  // row g+8, k = 2t+8, 2t+9 <- word 2t+1
-        mma_16816(c, a, xb[P], xb[F::kPairs + P], c);
+    static_for<F::kPairs>([&](auto sc) {
+        constexpr int S = decltype(sc)::value;
+        mma_16816(c,
+                  lane_pair<TYPE, 2 * S>(w00, s00, w10, s10),       // row g,   k = 2t, 2t+1
+                  lane_pair<TYPE, 2 * S>(w01, s01, w11, s11),       // row g+8, k = 2t, 2t+1
+                  lane_pair<TYPE, 2 * S + 1>(w00, s00, w10, s10),   // row g,   k = 2t+8, 2t+9
+                  lane_pair<TYPE, 2 * S + 1>(w01, s01, w11, s11),   // row g+8, k = 2t+8, 2t+9
+                  xb[2 * S], xb[2 * S + 1]);
     });
     part[0] = fmaf(d0, c[0], part[0]);
     part[2] = fmaf(d1, c[2], part[2]);
