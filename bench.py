@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--hadamard", type=int, default=0,
+                    help="rotate every tensor's activations with pn_hadamard (this block size) "
+                         "before its GEMV, inside each step (0 = off)")
     return ap.parse_args()
 
 
@@ -344,19 +347,24 @@ def run_ours(args, world, rank, local):
         del w
         xs = torch.from_numpy(synth.activations(synth.x_seed(args.config, e), M, K)).to(dev)
         sets.append((t, K, N, W0, xs))
+    # with --hadamard every tensor's GEMV reads a rotated copy of its activations
+    xr = [torch.empty_like(xs) for _, _, _, _, xs in sets] if args.hadamard else None
     rot = []
     for c in range(copies):
         entries = []
-        for t, K, N, W0, xs in sets:
+        for e, (t, K, N, W0, xs) in enumerate(sets):
             W = W0 if c == 0 else W0.clone()
             y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            entries.append((t, W, K, xs, y))
+            entries.append((t, W, K, xr[e] if xr is not None else xs, y))
         rot.append(entries)
     total_rows = sum(N for _, _, N in tensors)
     ws = pn.Workspace(total_rows, dev)
     stream = torch.cuda.Stream(device=dev)
 
     def step(entries):
+        if xr is not None:
+            for (_, _, _, _, xs), xo in zip(sets, xr):
+                pn.hadamard(xs, args.hadamard, out=xo, stream=stream)
         if len(entries) == 1:
             t, W, K, x, y = entries[0]
             pn.gemv(t, W, K, x, y=y, workspace=ws, algo=algo, stream=stream)
@@ -435,7 +443,8 @@ def run_ours(args, world, rank, local):
 
         def e2e_step(i):
             entries = rot[i % copies]
-            for (t, W, K, x, y), xhost in zip(entries, xh):
+            dests = [xs for _, _, _, _, xs in sets] if xr is not None else [x for _, _, _, x, _ in entries]
+            for x, xhost in zip(dests, xh):
                 x.copy_(xhost, non_blocking=True)
             step(entries)
             for (t, W, K, x, y), yhost in zip(entries, yh):
@@ -486,10 +495,12 @@ def run_ours(args, world, rank, local):
                    "l2": f"{copies} rotating weight copies ({copies * wbytes / 1e6:.0f} MB > 2x L2)",
                    "launch": f"CUDA graph of {nodes} steps, replayed",
                    "parallelism": "replicas" if world > 1 else "1 GPU",
-                   "algo": args.algo},
+                   "algo": args.algo,
+                   "hadamard_block": args.hadamard or None},
         "us_per_gemv": ms_per_step * 1e3,
         "pct_of_nominal_8tbs": per_gpu / NOMINAL_HBM_GBS * 100.0,
-        "gpu_launches": args.steps * (1 if len(tensors) == 1 or algo != pn.ALGO_CUDA_CORE else len(tensors)),
+        "gpu_launches": args.steps * ((1 if len(tensors) == 1 or algo != pn.ALGO_CUDA_CORE else len(tensors))
+                                      + (len(tensors) if args.hadamard else 0)),
         "roofline": roofline,
         "clocks": clock_info,
         "e2e": e2e,

@@ -249,6 +249,18 @@ pn_status pn_gemv_layer(const pn_gemv_desc* descs, int count, int M, void* works
     return pn_gemv_layer_ex(descs, count, M, workspace, workspace_bytes, PN_ALGO_AUTO, stream);
 }
 
+pn_status pn_hadamard(const uint16_t* x, int M, int64_t K, int block, uint16_t* out, pn_stream stream) {
+    if (M < 1 || M > 65535 || K <= 0 || block < 2 || block > 4096 || (block & (block - 1)) || K % block)
+        return PN_EINVAL;
+    if (!x || !out) return PN_EINVAL;
+    if (!aligned(x, 2) || !aligned(out, 2)) return PN_EALIGN;
+    const size_t bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
+    if (x != out && overlaps(x, bytes, out, bytes)) return PN_EINVAL;
+    if (K / block > INT32_MAX) return PN_EINVAL;
+    return pn::launch_hadamard(x, M, K, block, out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PN_OK : PN_ECUDA;
+}
+
 void pn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
 
 void pn_set_test_stall(int on) { g_test_stall.store(on ? 1 : 0); }

@@ -19,6 +19,10 @@ struct GemvTensor {
     int nb;                 // blocks per row (K / weights per block)
 };
 
+// Block Hadamard rotation of fp16 activations [M][K] (block = 2^m dividing K,
+// 2 <= block <= 4096); out may equal x.
+cudaError_t launch_hadamard(const uint16_t* x, int M, int64_t K, int block, uint16_t* out, cudaStream_t s);
+
 cudaError_t launch_unpack(int type, const void* W, int64_t N, int64_t nb, float* w, cudaStream_t s);
 cudaError_t launch_pack(int type, const float* w, int64_t N, int64_t nb, void* W, cudaStream_t s);
 

@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.pn_gemv_layer.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, vp]
             L.pn_gemv_layer_ex.restype = i32
             L.pn_gemv_layer_ex.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, i32, vp]
+            L.pn_hadamard.restype = i32
+            L.pn_hadamard.argtypes = [vp, i32, i64, i32, vp, vp]
             L.pn_set_wait_timeout_ns.restype = None
             L.pn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
             L.pn_set_test_stall.restype = None
@@ -194,6 +196,19 @@ def gemv_layer(entries, M: int, workspace: Workspace | None = None, algo: int = 
     _check(lib().pn_gemv_layer_ex(arr, len(entries), M, ws_ptr, ws_bytes, algo, _stream(stream)),
            "pn_gemv_layer")
     return [e[4] for e in entries]
+
+
+def hadamard(x: torch.Tensor, block: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Block Hadamard rotation of fp16 activations [M][K] (see pn_hadamard)."""
+    _require(x, torch.float16, "x")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    M, K = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _require(out, torch.float16, "out")
+    _check(lib().pn_hadamard(_ptr(x), M, K, block, _ptr(out), _stream(stream)), "pn_hadamard")
+    return out
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -197,6 +197,25 @@ pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const u
                           float* y, pn_stream stream);
 
 /*
+ * pn_hadamard: the runtime Hadamard rotation of the activations that reach the
+ * PN weights (tensorless docs, "Why a P100-native weight format", section "How
+ * Qwen3.8-27B-PN3 uses it"; the page gives no size or normalisation, read
+ * here as follows).  Every run of `block` consecutive activations of each of
+ * the M rows of x (fp16 [M][K]) is multiplied by the orthonormal Sylvester
+ * Hadamard matrix H_block / sqrt(block) (H_1 = [1], H_2n = [[H, H], [H, -H]]),
+ * written to out (fp16 [M][K]; out may equal x, otherwise the two must not
+ * overlap).  block is a power of two, 2 <= block <= 4096, dividing K;
+ * 1 <= M <= 65535.  Arithmetic, fixed so results are reproducible bit for
+ * bit: fp16 -> fp32; butterfly stages h = 1, 2, ..., block/2 in that order,
+ * each replacing (v[i], v[i+h]) for (i & h) == 0 by (v[i] + v[i+h],
+ * v[i] - v[i+h]) in fp32; one fp32 multiply by 2^(-m/2) (block = 2^m, m even)
+ * or 2^(-(m+1)/2) * fp32(sqrt 2) (m odd); fp16 round-to-nearest-even.  x and
+ * out 2-byte aligned.  Asynchronous on `stream`; a following pn_gemv on the
+ * same stream reads the rotated activations.
+ */
+pn_status pn_hadamard(const uint16_t* x, int M, int64_t K, int block, uint16_t* out, pn_stream stream);
+
+/*
  * Testing aid: the time limit, in nanoseconds, of every device-side wait in
  * the tensor-core kernel (default 1e9).  A wait that runs out stops its thread
  * block, which records PN_ETIMEOUT in the workspace status word and returns

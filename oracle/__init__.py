@@ -7,7 +7,9 @@ accumulation); this module compiles it with gcc and wraps it with ctypes over
 numpy arrays.
 
 Source: tensorless docs, "Why a P100-native weight format" (block layout,
-half-word packing, exact decode, mid-tread codes with a signed scale).
+half-word packing, exact decode, mid-tread codes with a signed scale; the
+runtime Hadamard rotation of the activations, section "How Qwen3.8-27B-PN3
+uses it").
 """
 from __future__ import annotations
 
@@ -68,6 +70,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_half_to_float.argtypes = [ctypes.c_uint16]
     lib.oracle_float_to_half.restype = ctypes.c_uint16
     lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+    lib.oracle_hadamard.restype = ctypes.c_int
+    lib.oracle_hadamard.argtypes = [c_void_p, ctypes.c_int, i64, ctypes.c_int, c_void_p, c_void_p]
     return lib
 
 
@@ -155,6 +159,22 @@ class Oracle:
             if hi > lo:
                 y[:, lo:hi] = parts[i]
         return y
+
+    def hadamard(self, x: np.ndarray, block: int, want_f32: bool = False):
+        """Block Hadamard rotation of fp16 activations [M][K] (reading R10):
+        returns fp16 [M][K] and, if asked, the fp32 values before rounding."""
+        x = np.ascontiguousarray(x, dtype=np.float16)
+        if x.ndim == 1:
+            x = x[None, :]
+        M, K = x.shape
+        out = np.empty((M, K), dtype=np.float16)
+        o32 = np.empty((M, K), dtype=np.float32) if want_f32 else None
+        rc = self.lib.oracle_hadamard(x.view(np.uint16).ctypes.data, M, K, block,
+                                      out.view(np.uint16).ctypes.data,
+                                      o32.ctypes.data if want_f32 else None)
+        if rc:
+            raise ValueError(f"oracle_hadamard failed ({rc})")
+        return (out, o32) if want_f32 else out
 
     def half_to_float(self, h: int) -> float:
         return float(self.lib.oracle_half_to_float(h))

@@ -267,3 +267,57 @@ int oracle_gemv(int type, const uint8_t* W, int64_t N, int64_t K,
     }
     return ORACLE_OK;
 }
+
+/* ---------------------------------------------------- Hadamard rotation --- */
+
+/*
+ * Runtime rotation of the activations that reach the PN weights (tensorless
+ * docs, "Why a P100-native weight format", section "How Qwen3.8-27B-PN3 uses
+ * it": the model applies a Hadamard rotation to those activations and the
+ * engine performs it at run time).  The page gives neither the size nor the
+ * normalisation of the rotation.  Reading R10: every run of B consecutive
+ * activations of a row (B = 2^m, 2 <= B <= 4096, B dividing K) is multiplied
+ * by the orthonormal Sylvester Hadamard matrix H_B / sqrt(B), where
+ * H_1 = [1] and H_2n = [[H_n, H_n], [H_n, -H_n]].
+ *
+ * The arithmetic is fixed so that results are reproducible bit for bit: each
+ * fp16 input is widened to fp32; the fast Walsh-Hadamard butterflies run in
+ * stages h = 1, 2, 4, ..., B/2, in that order, each stage replacing the pair
+ * (v[i], v[i+h]) for every i with (i & h) == 0 by (v[i] + v[i+h],
+ * v[i] - v[i+h]) in fp32; each result is multiplied once, in fp32, by
+ * s = 2^(-m/2) (m even) or s = 2^(-(m+1)/2) * fp32(sqrt(2)) (m odd, the
+ * constant rounded to nearest), and rounded to fp16 (nearest, ties to even).
+ *
+ * x, out: fp16 bit patterns [M][K] (out may equal x).  out32, if not NULL,
+ * receives the fp32 values before the final rounding.
+ */
+int oracle_hadamard(const uint16_t* x, int M, int64_t K, int B, uint16_t* out, float* out32)
+{
+    if (!x || !out || M < 1 || K <= 0 || B < 2 || B > 4096 || (B & (B - 1)) || K % B) return ORACLE_EINVAL;
+    int m = 0;
+    while ((1 << m) < B) ++m;
+    const float sqrt2 = 1.41421356237309504880f;          /* fp32 nearest to sqrt(2) */
+    float s = ldexpf(1.0f, -(m / 2));
+    if (m % 2) s = ldexpf(sqrt2, -(m + 1) / 2);
+    float v[4096];
+    for (int row = 0; row < M; ++row) {
+        for (int64_t base = 0; base < K; base += B) {
+            const int64_t off = (int64_t)row * K + base;
+            for (int i = 0; i < B; ++i) v[i] = oracle_half_to_float(x[off + i]);
+            for (int h = 1; h < B; h *= 2) {
+                for (int i = 0; i < B; ++i) {
+                    if (i & h) continue;
+                    const float a = v[i], b = v[i + h];
+                    v[i] = a + b;
+                    v[i + h] = a - b;
+                }
+            }
+            for (int i = 0; i < B; ++i) {
+                const float r = v[i] * s;
+                if (out32) out32[off + i] = r;
+                out[off + i] = oracle_float_to_half(r);
+            }
+        }
+    }
+    return ORACLE_OK;
+}

@@ -88,3 +88,32 @@ def assert_gemv_close(y, y_ref, abs_sum, rel=REL, abs_=ABS):
                            f"bound {bound[tuple(i)]:.3g}" for i in idx)
         raise AssertionError(f"{int(bad.sum())} of {bad.size} outputs out of tolerance: {detail}")
     return float(np.max(err / bound)) if err.size else 0.0
+
+
+def read_hadamard_cases():
+    """Parse tests/golden/hadamard_worked.txt: list of (name, block, x fp16, out bits)."""
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "hadamard_worked.txt")) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, val = line.partition(" ")
+            if key == "case":
+                cur = {"name": val}
+                cases.append(cur)
+            elif key == "block":
+                cur["block"] = int(val)
+            elif key == "x":
+                cur["x"] = np.array([float(v) for v in val.split()], dtype=np.float16)
+            elif key == "out":
+                cur["out"] = np.array([int(v, 16) for v in val.split()], dtype=np.uint16)
+    return cases
+
+
+def sylvester_hadamard(n: int) -> np.ndarray:
+    """H_n in Sylvester order (H_1 = [1], H_2n = [[H, H], [H, -H]]), fp64."""
+    h = np.ones((1, 1))
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h

@@ -89,3 +89,19 @@ def test_layer_checks(lib):
     assert lib.pn_gemv_layer(arr, 0, 1, FAKE * 32, 1 << 20, None) == PN_EINVAL
     assert lib.pn_gemv_layer(arr, 9, 1, FAKE * 32, 1 << 20, None) == PN_EINVAL
     assert lib.pn_gemv_layer(None, 1, 1, FAKE * 32, 1 << 20, None) == PN_EINVAL
+
+
+def test_hadamard_checks(lib):
+    h = lib.pn_hadamard
+    h.restype = ctypes.c_int
+    h.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    # block not a power of two, too small, too large, not dividing K; M out of range
+    assert h(FAKE, 1, 96, 3, FAKE * 2, None) == PN_EINVAL
+    assert h(FAKE, 1, 96, 1, FAKE * 2, None) == PN_EINVAL
+    assert h(FAKE, 1, 8192, 8192, FAKE * 2, None) == PN_EINVAL
+    assert h(FAKE, 1, 96, 64, FAKE * 2, None) == PN_EINVAL
+    assert h(FAKE, 0, 96, 32, FAKE * 2, None) == PN_EINVAL
+    # null, misaligned, partly overlapping buffers
+    assert h(None, 1, 96, 32, FAKE * 2, None) == PN_EINVAL
+    assert h(FAKE + 1, 1, 96, 32, FAKE * 2, None) == PN_EALIGN
+    assert h(FAKE, 1, 96, 32, FAKE + 64, None) == PN_EINVAL

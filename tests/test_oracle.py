@@ -22,7 +22,7 @@ import pytest
 
 import oracle as oracle_mod
 from helpers import (GEOMETRY, PN3T, PN4T, f16_bits_to_f64, on_grid_weights,
-                     read_worked_blocks)
+                     read_hadamard_cases, read_worked_blocks, sylvester_hadamard)
 
 TYPES = (PN3T, PN4T)
 
@@ -317,9 +317,59 @@ def pin_gemv_independent(o):
         assert np.all(np.abs(lhs - (y1 + y2)).T <= rounding + 1e-6 * (a1 + a2 + al).T)
 
 
+# ------------------------------------------------------ Hadamard rotation ----
+
+def pin_hadamard_worked(o):
+    # hand-derived rotations of small blocks (tests/golden/hadamard_worked.txt)
+    for case in read_hadamard_cases():
+        got = o.hadamard(case["x"][None, :], case["block"])[0]
+        assert np.array_equal(got.view(np.uint16), case["out"]), case["name"]
+
+
+def pin_hadamard_dense(o):
+    # the fp32 values before rounding equal H_B x / sqrt(B) computed densely in
+    # fp64 (Sylvester matrix by numpy) up to the fp32 rounding of log2(B)
+    # butterfly stages and one scale; the fp16 output is their rounding (numpy's)
+    rng = np.random.default_rng(23)
+    for B, K, M in ((2, 6, 2), (4, 12, 3), (8, 40, 2), (64, 192, 2), (1024, 2048, 2), (2048, 6144, 1),
+                    (4096, 8192, 1)):
+        x = rng.standard_normal((M, K)).astype(np.float16)
+        out, o32 = o.hadamard(x, B, want_f32=True)
+        m = int(math.log2(B))
+        xb = x.astype(np.float64).reshape(M, K // B, B)
+        ref = (xb @ sylvester_hadamard(B).T / math.sqrt(B)).reshape(M, K)
+        bound = (m + 2) * 2.0 ** -24 * (np.abs(xb).sum(axis=2, keepdims=True) / math.sqrt(B))
+        bound = np.broadcast_to(bound, xb.shape).reshape(M, K)
+        assert np.all(np.abs(o32.astype(np.float64) - ref) <= bound), B
+        assert np.array_equal(out.view(np.uint16), o32.astype(np.float16).view(np.uint16)), B
+
+
+def pin_hadamard_structure(o):
+    # one-hot rows give +-1/sqrt(B) everywhere; constant rows give sqrt(B) times
+    # the constant in slot 0 and zeros elsewhere; rotating twice gives x back
+    # up to the two fp16 roundings; a row's blocks are rotated independently
+    for B in (2, 4, 8, 16, 256, 2048):
+        K = 2 * B
+        e = np.zeros((1, K), dtype=np.float16)
+        e[0, B + 3 % B] = 1.0
+        _, o32 = o.hadamard(e, B, want_f32=True)
+        assert np.all(o32[0, :B] == 0.0)
+        assert np.allclose(np.abs(o32[0, B:]), 1.0 / math.sqrt(B), rtol=2.0 ** -22, atol=0)
+        c = np.full((1, K), 0.5, dtype=np.float16)
+        _, o32 = o.hadamard(c, B, want_f32=True)
+        for blk in range(2):
+            v = o32[0, blk * B:(blk + 1) * B].astype(np.float64)
+            assert v[0] == pytest.approx(0.5 * math.sqrt(B), rel=2.0 ** -22) and np.all(v[1:] == 0.0)
+        rng = np.random.default_rng(B)
+        x = rng.standard_normal((2, K)).astype(np.float16)
+        back = o.hadamard(o.hadamard(x, B), B).astype(np.float64)
+        assert np.all(np.abs(back - x.astype(np.float64)) <= 2.0 ** -9 * np.abs(x).max() * 4)
+
+
 ALL_PINS = [pin_block_geometry, pin_worked_blocks, pin_fp16_conversion, pin_decode_exact_all_scales,
             pin_half_structure, pin_every_half_round_trips, pin_full_range_and_bound,
-            pin_on_grid_lossless, pin_special_blocks, pin_gemv_exact_tiny, pin_gemv_independent]
+            pin_on_grid_lossless, pin_special_blocks, pin_gemv_exact_tiny, pin_gemv_independent,
+            pin_hadamard_worked, pin_hadamard_dense, pin_hadamard_structure]
 
 
 # ------------------------------------------------------------------- tests ----
@@ -335,6 +385,10 @@ def test_oracle_rejects_bad_arguments(oracle):
     with pytest.raises(ValueError):
         oracle.unpack(PN4T, np.zeros((2, 34), dtype=np.uint8), 80)
     assert oracle.lib.oracle_pack(99, None, 1, 80, None) != 0
+    x = np.zeros((1, 24), dtype=np.float16)
+    for block in (3, 1, 8192, 16):       # not a power of two, too small, too large, not dividing K
+        with pytest.raises(ValueError):
+            oracle.hadamard(x if block != 8192 else np.zeros((1, 8192), dtype=np.float16), block)
 
 
 def test_gemv_threads_match_single(oracle):
@@ -368,6 +422,10 @@ MUTATIONS = {
                            "for (int64_t b = 0; b + 1 < nb; ++b) {\n                decode_block"),
     "rows_reversed": ("y[(int64_t)m * N + r] = (float)acc;", "y[(int64_t)m * N + (N - 1 - r)] = (float)acc;"),
     "fp32_accumulate": ("double acc = 0.0, acc_abs = 0.0;", "float acc = 0.0f; double acc_abs = 0.0;"),
+    "hadamard_difference_sign": ("v[i + h] = a - b;", "v[i + h] = b - a;"),
+    "hadamard_odd_scale": ("if (m % 2) s = ldexpf(sqrt2, -(m + 1) / 2);", "if (m % 2) s = ldexpf(1.0f, -(m + 1) / 2);"),
+    "hadamard_block_offset": ("const int64_t off = (int64_t)row * K + base;", "const int64_t off = (int64_t)row * K;"),
+    "hadamard_partner": ("const float a = v[i], b = v[i + h];", "const float a = v[i], b = v[(i + h) % B];\n                    if (h > 1) continue;"),
 }
 
 
