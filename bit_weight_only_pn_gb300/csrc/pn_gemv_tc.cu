@@ -500,6 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     volatile uint32_t* abort_flag =
         reinterpret_cast<volatile uint32_t*>(smem + kBarrierOffset + kNumBarriers * 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // programmatic dependent launch: the next kernel may start now; this one
+    // touches activations, outputs and the workspace only after the previous
+    // kernel has finished (griddep_wait below), warming L2 with its first
+    // weights meanwhile
+    griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -532,6 +537,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         }
         Walker it;
         it.init(P, u0, u1);
+        if (!it.done && lane < kBatchTiles) {
+            // the first two steps' weight rows of the first batch, into L2
+            const Batch& b = it.cur;
+            const int j = lane >> b.lanes_log2, q = lane & (b.lanes - 1);
+            if (j < b.nt)
+                for (int k = 0; k < 2; ++k) {
+                    const int c = it.cstart + q + k * b.lanes;
+                    if (c < it.cend) tma_prefetch_l2_2d(&P.wmap[0][b.e], c * kBoxWords, (b.tb + j) * kTileRows);
+                }
+        }
+        griddep_wait();
         Ring ring;
         int idx = 0;
         bool stop = false;
@@ -622,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         // ------------------------------------------------------- epilogue --
         // Walks the same batches; when a batch's warp pairs have handed off
         // their sums it emits the batch.
+        griddep_wait();
         Walker it;
         it.init(P, u0, u1);
         uint32_t kcount[kBatchTiles];
@@ -655,6 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         }
     } else {
         // ------------------------------------------------------- consumers --
+        griddep_wait();
         const int slot = warp >> 1, half = warp & 1;
         const int xtoken = (lane >> 2) < P.M ? (lane >> 2) : 0;
         Walker it;
@@ -776,8 +794,17 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* stat
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    gemv_tc_kernel<<<P.grid, kThreads, kSmemBytes, s>>>(P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(P.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_tc_kernel, P);
 }
 
 }  // namespace pn
