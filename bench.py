@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4, 5])
     ap.add_argument("--algo", choices=["auto", "tc", "cuda_core"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

@@ -16,6 +16,7 @@ std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_cc_major[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_test_stall{0};
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;   // behind this thread's last PN_ECUDA
 
 int per_block(int type) { return type == PN_TYPE_PN3T ? 80 : (type == PN_TYPE_PN4T ? 64 : 0); }
 
@@ -29,6 +30,12 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }  // namespace
 
 namespace pn {
+pn_status cuda_error(cudaError_t e) {
+    g_last_cuda_error = e;
+    cudaGetLastError();             // clear it (a sticky error stays regardless)
+    return PN_ECUDA;
+}
+
 WorkspaceLayout workspace_layout(int num_sms) {
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
     WorkspaceLayout L;
@@ -46,16 +53,14 @@ namespace {
 // SM count and compute-capability major of the current device (cached).
 pn_status device_info(int* sms, int* major) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return PN_ECUDA; }
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return pn::cuda_error(e);
     if (dev < 0 || dev >= kMaxDevices) return PN_EUNSUPPORTED;
     int s = g_sm_count[dev].load(std::memory_order_relaxed);
     int m = g_cc_major[dev].load(std::memory_order_relaxed);
     if (s <= 0) {
-        if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&m, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return PN_ECUDA;
-        }
+        cudaError_t e = cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e != cudaSuccess) return pn::cuda_error(e);
         g_cc_major[dev].store(m, std::memory_order_relaxed);
         g_sm_count[dev].store(s, std::memory_order_relaxed);
     }
@@ -120,10 +125,10 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
             : pn::launch_gemv_tc(tc, ntc, M, status, reinterpret_cast<float*>(base + L.partials),
                                  reinterpret_cast<uint32_t*>(base + L.counters), sms, g_timeout_ns.load(),
                                  g_test_stall.load(), s);
-        if (e != cudaSuccess) return PN_ECUDA;
+        if (e != cudaSuccess) return pn::cuda_error(e);
     }
     for (int i = 0; i < nsimt; ++i)
-        if (pn::launch_gemv_simt(simt[i], M, s) != cudaSuccess) return PN_ECUDA;
+        if (cudaError_t e = pn::launch_gemv_simt(simt[i], M, s); e != cudaSuccess) return pn::cuda_error(e);
     return PN_OK;
 }
 
@@ -161,8 +166,8 @@ pn_status pn_pack(int type, const float* w, int64_t N, int64_t K, void* W, pn_st
     if (!aligned(w, 4) || !aligned(W, 2)) return PN_EALIGN;
     if (overlaps(w, static_cast<size_t>(N) * K * 4, W, static_cast<size_t>(N) * (K / bpb) * PN_BLOCK_BYTES))
         return PN_EINVAL;
-    return pn::launch_pack(type, w, N, K / bpb, W, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PN_OK : PN_ECUDA;
+    const cudaError_t e = pn::launch_pack(type, w, N, K / bpb, W, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
 }
 
 pn_status pn_unpack(int type, const void* W, int64_t N, int64_t K, float* w, pn_stream stream) {
@@ -173,8 +178,8 @@ pn_status pn_unpack(int type, const void* W, int64_t N, int64_t K, float* w, pn_
     if (!aligned(w, 4) || !aligned(W, 2)) return PN_EALIGN;
     if (overlaps(w, static_cast<size_t>(N) * K * 4, W, static_cast<size_t>(N) * (K / bpb) * PN_BLOCK_BYTES))
         return PN_EINVAL;
-    return pn::launch_unpack(type, W, N, K / bpb, w, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PN_OK : PN_ECUDA;
+    const cudaError_t e = pn::launch_unpack(type, W, N, K / bpb, w, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
 }
 
 size_t pn_workspace_bytes(int64_t total_rows) {
@@ -185,21 +190,19 @@ size_t pn_workspace_bytes(int64_t total_rows) {
 
 pn_status pn_workspace_init(void* workspace, size_t workspace_bytes, pn_stream stream) {
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return PN_EINVAL;
-    return cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PN_OK : PN_ECUDA;
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
 }
 
 pn_status pn_workspace_status(void* workspace, size_t workspace_bytes, pn_stream stream) {
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return PN_EINVAL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t word = 0;
-    if (cudaStreamSynchronize(s) != cudaSuccess ||
-        cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
-        cudaGetLastError();
-        return PN_ECUDA;
-    }
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return pn::cuda_error(e);
     if (word == 0) return PN_OK;
-    if (cudaMemset(workspace, 0, workspace_bytes) != cudaSuccess) { cudaGetLastError(); return PN_ECUDA; }
+    if (cudaError_t e2 = cudaMemset(workspace, 0, workspace_bytes); e2 != cudaSuccess) return pn::cuda_error(e2);
     return word == PN_ETIMEOUT ? PN_ETIMEOUT : PN_ECUDA;
 }
 
@@ -257,9 +260,11 @@ pn_status pn_hadamard(const uint16_t* x, int M, int64_t K, int block, uint16_t* 
     const size_t bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
     if (x != out && overlaps(x, bytes, out, bytes)) return PN_EINVAL;
     if (K / block > INT32_MAX) return PN_EINVAL;
-    return pn::launch_hadamard(x, M, K, block, out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? PN_OK : PN_ECUDA;
+    const cudaError_t e = pn::launch_hadamard(x, M, K, block, out, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
 }
+
+const char* pn_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 void pn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
 

@@ -279,15 +279,16 @@ __device__ __forceinline__ uint32_t lane_pair(uint32_t w0, uint32_t s0, uint32_t
     else return decode_pair<TYPE, Q - kP>(w1, s1);
 }
 
-// Block B of staged rows r0 (MMA row g) and r1 (row g + 8) times the lane's x
-// pairs xb (xb[q] pairs with code pair q, see above).  The block's products
-// start from zero and are scaled by the rows' d in fp32:
-// part[0..1] += d(r0) * (columns 2t, 2t+1), part[2..3] += d(r1) * (same).
-// With kOddCols false the odd columns (part[1], part[3]) are left alone, for
-// callers that only read even columns (a single token).
-template <int TYPE, int B, bool kOddCols = true>
-__device__ __forceinline__ void block_mma(const uint8_t* r0, const uint8_t* r1, int t,
-                                          const uint32_t (&xb)[2 * Format<TYPE>::kPairs], float (&part)[4]) {
+// Block B of staged rows r0 (MMA row g) and r1 (row g + 8) times NT column
+// tiles of x (tokens 8n .. 8n+7 in tile n).  xpair(n, S) gives the lane's two
+// B-fragment registers of MMA S in tile n: the x pairs that go with code
+// pairs 2S and 2S + 1 of lane_pair's numbering.  The A fragments are decoded
+// once and feed one MMA per column tile.  Each block's products start from
+// zero and are scaled by the rows' d in fp32: part[n][0..1] += d(r0) *
+// (columns 2t, 2t+1 of tile n), part[n][2..3] += d(r1) * (same).
+template <int TYPE, int B, int NT, typename XPair>
+__device__ __forceinline__ void block_mma(const uint8_t* r0, const uint8_t* r1, int t, XPair&& xpair,
+                                          float (&part)[NT][4]) {
     using F = Format<TYPE>;
     const float d0 = lds_half_as_float(r0 + B * kBlockBytes);
     const float d1 = lds_half_as_float(r1 + B * kBlockBytes);
@@ -296,21 +297,27 @@ __device__ __forceinline__ void block_mma(const uint8_t* r0, const uint8_t* r1, 
     load_words<B>(r1, t, w01, w11);
     const uint32_t s00 = w00 >> F::kHighShift, s10 = w10 >> F::kHighShift;
     const uint32_t s01 = w01 >> F::kHighShift, s11 = w11 >> F::kHighShift;
-    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float c[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) c[n][0] = c[n][1] = c[n][2] = c[n][3] = 0.0f;
     static_for<F::kPairs>([&](auto sc) {
         constexpr int S = decltype(sc)::value;
-        mma_16816(c,
-                  lane_pair<TYPE, 2 * S>(w00, s00, w10, s10),       // row g,   k = 2t, 2t+1
-                  lane_pair<TYPE, 2 * S>(w01, s01, w11, s11),       // row g+8, k = 2t, 2t+1
-                  lane_pair<TYPE, 2 * S + 1>(w00, s00, w10, s10),   // row g,   k = 2t+8, 2t+9
-                  lane_pair<TYPE, 2 * S + 1>(w01, s01, w11, s11),   // row g+8, k = 2t+8, 2t+9
-                  xb[2 * S], xb[2 * S + 1]);
+        const uint32_t a0 = lane_pair<TYPE, 2 * S>(w00, s00, w10, s10);       // row g,   k = 2t, 2t+1
+        const uint32_t a1 = lane_pair<TYPE, 2 * S>(w01, s01, w11, s11);       // row g+8, k = 2t, 2t+1
+        const uint32_t a2 = lane_pair<TYPE, 2 * S + 1>(w00, s00, w10, s10);   // row g,   k = 2t+8, 2t+9
+        const uint32_t a3 = lane_pair<TYPE, 2 * S + 1>(w01, s01, w11, s11);   // row g+8, k = 2t+8, 2t+9
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const uint2 b = xpair(n, sc);
+            mma_16816(c[n], a0, a1, a2, a3, b.x, b.y);
+        }
     });
-    part[0] = fmaf(d0, c[0], part[0]);
-    part[2] = fmaf(d1, c[2], part[2]);
-    if constexpr (kOddCols) {
-        part[1] = fmaf(d0, c[1], part[1]);
-        part[3] = fmaf(d1, c[3], part[3]);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        part[n][0] = fmaf(d0, c[n][0], part[n][0]);
+        part[n][1] = fmaf(d0, c[n][1], part[n][1]);
+        part[n][2] = fmaf(d1, c[n][2], part[n][2]);
+        part[n][3] = fmaf(d1, c[n][3], part[n][3]);
     }
 }
 

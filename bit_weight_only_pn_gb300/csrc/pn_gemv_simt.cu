@@ -21,7 +21,8 @@ namespace {
 
 constexpr int kWarps = 8;
 
-template <int TYPE>
+// MAXM: accumulators per lane (8 or 16), at least M.
+template <int TYPE, int MAXM>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_simt_kernel(const uint8_t* __restrict__ W, int N, int nb, const uint16_t* __restrict__ x,
                  int M, float* __restrict__ y) {
@@ -32,9 +33,9 @@ gemv_simt_kernel(const uint8_t* __restrict__ W, int N, int nb, const uint16_t* _
     const int64_t halves_per_row = static_cast<int64_t>(nb) * (kBlockBytes / 2);
     const int words = nb * kWordsPerBlock;
     for (int row = blockIdx.x * kWarps + (threadIdx.x >> 5); row < N; row += gridDim.x * kWarps) {
-        float acc[kMaxM];
+        float acc[MAXM];
 #pragma unroll
-        for (int m = 0; m < kMaxM; ++m) acc[m] = 0.0f;
+        for (int m = 0; m < MAXM; ++m) acc[m] = 0.0f;
         const uint16_t* rw = W16 + row * halves_per_row;
         for (int wi = lane; wi < words; wi += 32) {
             const int blk = wi >> 3, j = wi & 7;
@@ -43,16 +44,16 @@ gemv_simt_kernel(const uint8_t* __restrict__ W, int N, int nb, const uint16_t* _
             const uint32_t word = static_cast<uint32_t>(__ldg(bp + 1 + 2 * j)) |
                                   (static_cast<uint32_t>(__ldg(bp + 2 + 2 * j)) << 16);
             const int k0 = blk * F::kPerBlock + j * F::kPerWord;
-            float part[kMaxM];
+            float part[MAXM];
 #pragma unroll
-            for (int m = 0; m < kMaxM; ++m) part[m] = 0.0f;
+            for (int m = 0; m < MAXM; ++m) part[m] = 0.0f;
 #pragma unroll
             for (int c = 0; c < F::kPerWord; ++c) {
                 const int shift = 16 * (c & 1) + F::kBits * (c >> 1);
                 const float v = static_cast<float>(
                     static_cast<int>((word >> shift) & ((1u << F::kBits) - 1u)) - F::kZero);
 #pragma unroll
-                for (int m = 0; m < kMaxM; ++m) {
+                for (int m = 0; m < MAXM; ++m) {
                     if (m < M) {
                         const float xv = __half2float(__ushort_as_half(__ldg(x + (int64_t)m * K + k0 + c)));
                         part[m] = fmaf(v, xv, part[m]);    // (n - z) * x is exact in fp32
@@ -60,10 +61,10 @@ gemv_simt_kernel(const uint8_t* __restrict__ W, int N, int nb, const uint16_t* _
                 }
             }
 #pragma unroll
-            for (int m = 0; m < kMaxM; ++m) acc[m] = fmaf(d, part[m], acc[m]);
+            for (int m = 0; m < MAXM; ++m) acc[m] = fmaf(d, part[m], acc[m]);
         }
 #pragma unroll
-        for (int m = 0; m < kMaxM; ++m) {
+        for (int m = 0; m < MAXM; ++m) {
             if (m < M) {
                 float v = acc[m];
 #pragma unroll
@@ -79,10 +80,13 @@ gemv_simt_kernel(const uint8_t* __restrict__ W, int N, int nb, const uint16_t* _
 cudaError_t launch_gemv_simt(const GemvTensor& t, int M, cudaStream_t s) {
     int64_t blocks = (static_cast<int64_t>(t.N) + kWarps - 1) / kWarps;
     const int grid = static_cast<int>(blocks > 65535 * 8 ? 65535 * 8 : (blocks < 1 ? 1 : blocks));
-    if (t.type == kPn3t)
-        gemv_simt_kernel<kPn3t><<<grid, kWarps * 32, 0, s>>>(t.W, t.N, t.nb, t.x, M, t.y);
-    else
-        gemv_simt_kernel<kPn4t><<<grid, kWarps * 32, 0, s>>>(t.W, t.N, t.nb, t.x, M, t.y);
+    if (t.type == kPn3t) {
+        if (M <= 8) gemv_simt_kernel<kPn3t, 8><<<grid, kWarps * 32, 0, s>>>(t.W, t.N, t.nb, t.x, M, t.y);
+        else gemv_simt_kernel<kPn3t, 16><<<grid, kWarps * 32, 0, s>>>(t.W, t.N, t.nb, t.x, M, t.y);
+    } else {
+        if (M <= 8) gemv_simt_kernel<kPn4t, 8><<<grid, kWarps * 32, 0, s>>>(t.W, t.N, t.nb, t.x, M, t.y);
+        else gemv_simt_kernel<kPn4t, 16><<<grid, kWarps * 32, 0, s>>>(t.W, t.N, t.nb, t.x, M, t.y);
+    }
     return cudaGetLastError();
 }
 

@@ -3,10 +3,12 @@
 //
 // What is computed: y[m][r] = sum_k d_blk(r,k) * (n(r,k) - z) * x[m][k], the
 // decode GEMV of the tensorless docs ("Why a P100-native weight format": "One
-// lane, one word", "Exact decode in fp32") at M = 1 and its skinny M <= 8 form
+// lane, one word", "Exact decode in fp32") in its skinny M = 3 .. 16 form
 // (speculative verification of k drafts in one batch, v100-skinny README, "How
 // QPN works": packed weights stay compressed through HBM and are decoded at the
-// point of consumption, straight into tensor-core register operands).
+// point of consumption, straight into tensor-core register operands; M = 9 ..
+// 16 is the band that README's "Where it stands" leaves to two 8-token tiles
+// per weight pass).
 //
 // Design (GB300-first; the pages' sm_60 and sm_70 kernels are prior art):
 //  * Work unit = one 16-row tile x one 8-block chunk (8 x 34 = 272 bytes per
@@ -35,6 +37,10 @@
 //    as B fragments straight from the staged chunk; each block's product sum
 //    starts from zero and is scaled by its d in fp32, so every product is
 //    exact and every sum is an fp32 sum.
+//  * M = 9 .. 16 runs the same kernel with two 8-column tiles (NT = 2): each
+//    decoded A fragment feeds two MMAs, one per 8 tokens, so the weights
+//    still cross HBM once; the stage holds 16 activation rows and the ring
+//    has three stages instead of four to stay within shared memory.
 #include <cstdint>
 
 #include <cuda.h>
@@ -63,25 +69,36 @@ constexpr int kTileBytes = kTileRows * kRowPitch;       // 4352
 constexpr int kStageWBytes = kBatchTiles * kTileBytes;  // 34816
 constexpr int kXPitchPn3t = kChunkBlocks * 80 * 2 + 16; // 1296
 constexpr int kXPitchPn4t = kChunkBlocks * 64 * 2 + 16; // 1040
-// Activations: one block of M rows per chunk lane, each block 128-byte aligned
-// (a tiled TMA destination); lanes * M <= 8, so 8 blocks of one row of the
-// pn3t pitch rounded up to 128 bytes always fit.
-constexpr int kStageXBytes = 8 * ((kXPitchPn3t + 127) / 128 * 128);   // 11264
-constexpr int kStageBytes = kStageWBytes + kStageXBytes;
-constexpr int kStages = 4;
-// Finished tile sums handed to the epilogue warp: [tile][buffer][half][lane] float4.
+constexpr int kXRowBytes = (kXPitchPn3t + 127) / 128 * 128;   // 1408
 constexpr int kOutBuffers = 2;
-constexpr int kOutOffset = kStages * kStageBytes;
-constexpr int kOutBytes = kBatchTiles * kOutBuffers * kTileWarps * 32 * 16;
-constexpr int kBarrierOffset = kOutOffset + kOutBytes;
-constexpr int kNumBarriers = 2 * kStages + 2 * kBatchTiles * kOutBuffers;
-constexpr int kSmemBytes = kBarrierOffset + kNumBarriers * 8 + 16;
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                  // PN_ETIMEOUT
-constexpr int kSlotFloats = kTileRows * kMaxM;          // 128: one tile's partial sums
+constexpr int kSlotFloats = kTileRows * kMaxM;          // 256: one tile's partial sums
 
-static_assert(kStageWBytes % 128 == 0 && kStageBytes % 128 == 0, "TMA destinations stay aligned");
-static_assert(kMaxM * kXPitchPn3t <= kStageXBytes, "one block of 8 activation rows fits");
+// Shared-memory layout of the kernel with NT 8-column tiles (M <= 8 NT).
+template <int NT>
+struct Smem {
+    // Activations: one block of M rows per chunk lane, each block 128-byte
+    // aligned (a tiled TMA destination); lanes * M <= 8 NT, so 8 NT rows of
+    // the pn3t pitch rounded up to 128 bytes always fit.
+    static constexpr int kXRows = 8 * NT;
+    static constexpr int kStageXBytes = kXRows * kXRowBytes;       // 11264 / 22528
+    static constexpr int kStageBytes = kStageWBytes + kStageXBytes;
+    static constexpr int kStages = NT == 1 ? 4 : 3;
+    // Finished tile sums handed to the epilogue warp:
+    // [tile][buffer][half][column tile][lane] float4.
+    static constexpr int kOutOffset = kStages * kStageBytes;
+    static constexpr int kOutBytes = kBatchTiles * kOutBuffers * kTileWarps * NT * 32 * 16;
+    static constexpr int kBarrierOffset = kOutOffset + kOutBytes;
+    static constexpr int kNumBarriers = 2 * kStages + 2 * kBatchTiles * kOutBuffers;
+    static constexpr int kBytes = kBarrierOffset + kNumBarriers * 8 + 16;
+    static_assert(kStageBytes % 128 == 0, "TMA destinations stay aligned");
+    static_assert(kXRows * kXPitchPn3t <= kStageXBytes, "one block of 8 NT activation rows fits");
+    static_assert(kBytes <= 227 * 1024, "fits one SM's shared memory");
+};
+
+static_assert(kStageWBytes % 128 == 0, "TMA destinations stay aligned");
+static_assert(2 * 8 <= kMaxM, "partial-sum slots hold 16 tokens");
 
 // Bytes between the activation blocks of consecutive chunk lanes.
 __host__ __device__ constexpr int x_block_bytes(int M, int pitch) { return (M * pitch + 127) / 128 * 128; }
@@ -109,6 +126,7 @@ struct TcParams {
     TcTensor t[kMaxLayer];
     int count;
     int M;
+    int x_rows;                    // activation rows a stage holds (8 per column tile)
     int grid;
     uint32_t units;                // units * grid < 2^32 (checked on the host)
     uint32_t* status;
@@ -174,9 +192,9 @@ struct Walker {
         b.nt = nt;
         b.cs0 = (e == e0 && tb == t0) ? c0 : 0;
         b.ce_last = (e == e1 && tb + nt - 1 == t1) ? c1e : P.t[e].chunks;
-        // chunk lanes: a power of two, as many as the 8 warp pairs and the 8
+        // chunk lanes: a power of two, as many as the 8 warp pairs and the
         // staged activation rows allow, no more than the tile has chunks
-        const int cap = min(min(kBatchTiles / nt, kMaxM / P.M), P.t[e].chunks);
+        const int cap = min(min(kBatchTiles / nt, P.x_rows / P.M), P.t[e].chunks);
         b.lanes_log2 = cap >= 8 ? 3 : cap >= 4 ? 2 : cap >= 2 ? 1 : 0;
         b.lanes = 1 << b.lanes_log2;
         b.chunks = P.t[e].chunks;
@@ -218,12 +236,13 @@ struct Walker {
     }
 };
 
-// Position in the stage ring.
+// Position in a ring of STAGES stages.
+template <int STAGES>
 struct Ring {
     int s = 0;
     uint32_t phase = 0;
     __device__ void advance() {
-        if (++s == kStages) { s = 0; phase ^= 1u; }
+        if (++s == STAGES) { s = 0; phase ^= 1u; }
     }
 };
 
@@ -290,67 +309,122 @@ __device__ __forceinline__ void load_x(const uint8_t* xrow, int t, uint32_t (&xb
 }
 
 // One consumer warp: the 16 rows of its tile times blocks 4H .. 4H+3 of a
-// chunk (the other warp of the pair takes the other four).  The scaled block
-// sums are added up per call and then added to the running sum, which keeps
-// every fp32 summation chain short (at most 4 block terms + one term per
-// chunk) whatever K is.  xrow is this lane's activation row; lanes whose MMA
-// column is past M read token 0 (a B column only feeds its own, unused,
-// output column), so no lane takes a different path.
-template <int TYPE, int H>
-__device__ __forceinline__ void mma_tile_half(const uint8_t* tile, const uint8_t* xrow, int lane,
-                                              float (&acc)[4]) {
+// chunk (the other warp of the pair takes the other four), for NT column
+// tiles of 8 tokens.  The scaled block sums are added up per call and then
+// added to the running sum, which keeps every fp32 summation chain short (at
+// most 4 block terms + one term per chunk) whatever K is.  xrow[n] is this
+// lane's activation row in column tile n; lanes whose MMA column is past M
+// read token 0 (a B column only feeds its own, unused, output column), so no
+// lane takes a different path.
+template <int TYPE, int H, int NT>
+__device__ __forceinline__ void mma_tile_half(const uint8_t* tile, const uint8_t* const (&xrow)[NT], int lane,
+                                              float (&acc)[NT][4]) {
     using F = Format<TYPE>;
     const int g = lane >> 2, t = lane & 3;
     const uint8_t* r0 = tile + tile_row(g) * kRowPitch;
     const uint8_t* r1 = r0 + 8 * kRowPitch;
-    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float part[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) part[n][0] = part[n][1] = part[n][2] = part[n][3] = 0.0f;
     static_for<kWarpBlocks>([&](auto bc) {
         constexpr int B = H * kWarpBlocks + decltype(bc)::value;
-        uint32_t xb[2 * F::kPairs];
-        load_x<TYPE, B>(xrow, t, xb);
-        block_mma<TYPE, B>(r0, r1, t, xb, part);
+        if constexpr (NT == 1) {
+            // one column tile: the block's x pairs are loaded up front
+            uint32_t xb[2 * F::kPairs];
+            load_x<TYPE, B>(xrow[0], t, xb);
+            block_mma<TYPE, B, 1>(r0, r1, t, [&](int, auto sc) {
+                constexpr int S = decltype(sc)::value;
+                return make_uint2(xb[2 * S], xb[2 * S + 1]);
+            }, part);
+        } else {
+            // two: each MMA's pairs are loaded next to it (one 64-bit load per
+            // MMA and tile), which keeps the operands within 96 registers
+            const int xoff = (B * F::kPerBlock + 2 * F::kPerWord * t) * 2;
+            block_mma<TYPE, B, NT>(r0, r1, t, [&](int n, auto sc) {
+                constexpr int S = decltype(sc)::value;
+                return lds_u64(xrow[n] + xoff + 8 * S);
+            }, part);
+        }
     });
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] += part[i];
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[n][i] += part[n][i];
 }
 
 // ------------------------------------------------------------------ flush --
 
-// Row of a tile that fragment row g (and g + 8) reads, see tile_row.
+// Row of a tile that fragment row g (and g + 8) reads, see tile_row.  v[n]
+// holds tokens 8n + 2t, 8n + 2t + 1 of rows g and g + 8.
+template <int NT>
 __device__ __forceinline__ void store_tile(const TcTensor& T, int M, int tile, int lane,
-                                           const float (&v)[4]) {
+                                           const float (&v)[NT][4]) {
     const int row0 = tile * kTileRows + tile_row(lane >> 2);
-    const int m0 = 2 * (lane & 3);
     const int rows[2] = {row0, row0 + 8};
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        if (rows[h] < T.N) {
-            if (m0 < M) T.y[static_cast<int64_t>(m0) * T.N + rows[h]] = v[2 * h];
-            if (m0 + 1 < M) T.y[static_cast<int64_t>(m0 + 1) * T.N + rows[h]] = v[2 * h + 1];
+    for (int n = 0; n < NT; ++n) {
+        const int m0 = 8 * n + 2 * (lane & 3);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (rows[h] < T.N) {
+                if (m0 < M) T.y[static_cast<int64_t>(m0) * T.N + rows[h]] = v[n][2 * h];
+                if (m0 + 1 < M) T.y[static_cast<int64_t>(m0 + 1) * T.N + rows[h]] = v[n][2 * h + 1];
+            }
         }
     }
 }
 
 // Partial sums of the tile shared across CTA boundary b (between CTA b-1 and
-// CTA b): side 0 holds CTA b-1's part (the tile's first chunks), side 1 CTA b's.
+// CTA b): side 0 holds CTA b-1's part (the tile's first chunks), side 1 CTA
+// b's; [row][token], kMaxM tokens per row.
 __device__ __forceinline__ float* slot_ptr(const TcParams& P, int boundary, int side) {
     return P.partials + (static_cast<int64_t>(boundary) * 2 + side) * kSlotFloats;
 }
 
-__device__ __forceinline__ uint32_t out_slot(uint32_t sbase, int tile, int buf, int half, int lane) {
-    return sbase + kOutOffset + (((tile * kOutBuffers + buf) * kTileWarps + half) * 32 + lane) * 16;
+// Writes / reads this lane's values of a tile to / from a partial-sum slot.
+template <int NT>
+__device__ __forceinline__ void slot_store(float* s, int lane, const float (&v)[NT][4]) {
+    const int r = lane >> 2;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const int m0 = 8 * n + 2 * (lane & 3);
+        __stcg(reinterpret_cast<float2*>(s + r * kMaxM + m0), make_float2(v[n][0], v[n][1]));
+        __stcg(reinterpret_cast<float2*>(s + (r + 8) * kMaxM + m0), make_float2(v[n][2], v[n][3]));
+    }
+}
+template <int NT>
+__device__ __forceinline__ void slot_load(const float* s, int lane, float (&v)[NT][4]) {
+    const int r = lane >> 2;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const int m0 = 8 * n + 2 * (lane & 3);
+        const float2 a = __ldcg(reinterpret_cast<const float2*>(s + r * kMaxM + m0));
+        const float2 b = __ldcg(reinterpret_cast<const float2*>(s + (r + 8) * kMaxM + m0));
+        v[n][0] = a.x; v[n][1] = a.y; v[n][2] = b.x; v[n][3] = b.y;
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ uint32_t out_slot(uint32_t sbase, int tile, int buf, int half, int n, int lane) {
+    return sbase + Smem<NT>::kOutOffset + ((((tile * kOutBuffers + buf) * kTileWarps + half) * NT + n) * 32 + lane) * 16;
 }
 
 // The finished sums of warp pair p (first half + second half, in that
 // order), read from the hand-off slots in shared memory.
-__device__ __forceinline__ void tile_sum(uint32_t sbase, int j, int buf, int lane, float (&v)[4]) {
-    float a[4], b[4];
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3]) : "r"(out_slot(sbase, j, buf, 0, lane)) : "memory");
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(b[0]), "=f"(b[1]), "=f"(b[2]), "=f"(b[3]) : "r"(out_slot(sbase, j, buf, 1, lane)) : "memory");
+template <int NT>
+__device__ __forceinline__ void tile_sum(uint32_t sbase, int j, int buf, int lane, float (&v)[NT][4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = a[i] + b[i];
+    for (int n = 0; n < NT; ++n) {
+        float a[4], b[4];
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3])
+                     : "r"(out_slot<NT>(sbase, j, buf, 0, n, lane)) : "memory");
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(b[0]), "=f"(b[1]), "=f"(b[2]), "=f"(b[3])
+                     : "r"(out_slot<NT>(sbase, j, buf, 1, n, lane)) : "memory");
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[n][i] = a[i] + b[i];
+    }
 }
 
 // Emits the tiles of batch `b` from the epilogue warp.  Whole tiles are
@@ -358,48 +432,50 @@ __device__ __forceinline__ void tile_sum(uint32_t sbase, int j, int buf, int lan
 // fence the (at most two) boundary counters are bumped together; where this
 // CTA arrived second it loads the neighbour's part and stores left + right.
 // `bufs` holds each warp pair's hand-off buffer index in bit p.
+template <int NT>
 __device__ void flush_batch(const TcParams& P, const Batch& b, int lane, uint32_t sbase, uint32_t bufs) {
     const TcTensor& T = P.t[b.e];
     const int cta = blockIdx.x;
-    const int r = lane >> 2, m0 = 2 * (lane & 3);
     const bool left_cut = b.cs0 > 0;                 // tile 0 began in CTA cta-1
     const bool right_cut = b.ce_last < T.chunks;     // tile nt-1 ends in CTA cta+1
-    float vl[4] = {0.0f, 0.0f, 0.0f, 0.0f}, vr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
+    float vl[NT][4], vr[NT][4];
+    // (the two-tile form keeps this loop rolled: unrolled, its sums do not
+    // fit the 96 registers)
+#pragma unroll (NT == 1 ? kBatchTiles : 1)
     for (int j = 0; j < kBatchTiles; ++j) {
         if (j >= b.nt) continue;
-        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int q = 0; q < b.lanes; ++q) {          // the tile's chunk lanes, in order
-            float w[4];
-            const int p = j * b.lanes + q;
-            tile_sum(sbase, p, (bufs >> p) & 1u, lane, w);
+        float v[NT][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] += w[i];
+        for (int n = 0; n < NT; ++n) v[n][0] = v[n][1] = v[n][2] = v[n][3] = 0.0f;
+        for (int q = 0; q < b.lanes; ++q) {          // the tile's chunk lanes, in order
+            float w[NT][4];
+            const int p = j * b.lanes + q;
+            tile_sum<NT>(sbase, p, (bufs >> p) & 1u, lane, w);
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[n][i] += w[n][i];
         }
         const bool lc = left_cut && j == 0, rc = right_cut && j == b.nt - 1;
         if (lc) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) vl[i] = v[i];
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vl[n][i] = v[n][i];
         } else if (rc) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) vr[i] = v[i];
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vr[n][i] = v[n][i];
         } else {
-            store_tile(T, P.M, b.tb + j, lane, v);
+            store_tile<NT>(T, P.M, b.tb + j, lane, v);
         }
     }
     if (!left_cut && !right_cut) return;
     // deposit: our part of the left-cut tile is side 1 of boundary cta; of the
     // right-cut tile, side 0 of boundary cta + 1
-    if (left_cut) {
-        float* s = slot_ptr(P, cta, 1);
-        __stcg(reinterpret_cast<float2*>(s + r * kMaxM + m0), make_float2(vl[0], vl[1]));
-        __stcg(reinterpret_cast<float2*>(s + (r + 8) * kMaxM + m0), make_float2(vl[2], vl[3]));
-    }
-    if (right_cut) {
-        float* s = slot_ptr(P, cta + 1, 0);
-        __stcg(reinterpret_cast<float2*>(s + r * kMaxM + m0), make_float2(vr[0], vr[1]));
-        __stcg(reinterpret_cast<float2*>(s + (r + 8) * kMaxM + m0), make_float2(vr[2], vr[3]));
-    }
+    if (left_cut) slot_store<NT>(slot_ptr(P, cta, 1), lane, vl);
+    if (right_cut) slot_store<NT>(slot_ptr(P, cta + 1, 0), lane, vr);
     __threadfence();
     __syncwarp();
     uint32_t old = 0;
@@ -409,25 +485,24 @@ __device__ void flush_batch(const TcParams& P, const Batch& b, int lane, uint32_
     const bool r_last = right_cut && __shfl_sync(0xFFFFFFFFu, old, 1) == 1u;
     if (!l_last && !r_last) return;
     __threadfence();
-    float2 la = make_float2(0.0f, 0.0f), lb = la, ra = la, rb = la;
-    if (l_last) {                                    // neighbour's part: side 0 of boundary cta
-        const float* s = slot_ptr(P, cta, 0);
-        la = __ldcg(reinterpret_cast<const float2*>(s + r * kMaxM + m0));
-        lb = __ldcg(reinterpret_cast<const float2*>(s + (r + 8) * kMaxM + m0));
-    }
-    if (r_last) {                                    // neighbour's part: side 1 of boundary cta+1
-        const float* s = slot_ptr(P, cta + 1, 1);
-        ra = __ldcg(reinterpret_cast<const float2*>(s + r * kMaxM + m0));
-        rb = __ldcg(reinterpret_cast<const float2*>(s + (r + 8) * kMaxM + m0));
-    }
     if (l_last) {                                    // left part (cta-1) + right part (cta)
-        const float v[4] = {la.x + vl[0], la.y + vl[1], lb.x + vl[2], lb.y + vl[3]};
-        store_tile(T, P.M, b.tb, lane, v);
+        float o[NT][4], v[NT][4];
+        slot_load<NT>(slot_ptr(P, cta, 0), lane, o);
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[n][i] = o[n][i] + vl[n][i];
+        store_tile<NT>(T, P.M, b.tb, lane, v);
         if (lane == 0) atomicExch(P.counters + cta, 0u);
     }
     if (r_last) {                                    // left part (cta) + right part (cta+1)
-        const float v[4] = {vr[0] + ra.x, vr[1] + ra.y, vr[2] + rb.x, vr[3] + rb.y};
-        store_tile(T, P.M, b.tb + b.nt - 1, lane, v);
+        float o[NT][4], v[NT][4];
+        slot_load<NT>(slot_ptr(P, cta + 1, 1), lane, o);
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[n][i] = vr[n][i] + o[n][i];
+        store_tile<NT>(T, P.M, b.tb + b.nt - 1, lane, v);
         if (lane == 0) atomicExch(P.counters + cta + 1, 0u);
     }
 }
@@ -444,27 +519,31 @@ struct Barriers {
 
 // Consumer side of a tile hand-off: the k-th finished sum of `tile` goes to
 // buffer k % 2 once the epilogue has emptied that buffer's previous use.
+template <int NT>
 __device__ bool handoff(const TcParams& P, const Barriers& B, uint32_t sbase, int tile, int half,
-                        int lane, uint32_t k, const float (&acc)[4], volatile uint32_t* abort_flag) {
+                        int lane, uint32_t k, const float (&acc)[NT][4], volatile uint32_t* abort_flag) {
     const int buf = k & 1u;
     const uint32_t use = k >> 1;
     if (use > 0 && !warp_wait(B.out_free(tile, buf), (use - 1) & 1u, P.timeout_ns, abort_flag, lane)) {
         if (lane == 0) raise_timeout(P, abort_flag);
         return false;
     }
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                 :: "r"(out_slot(sbase, tile, buf, half, lane)), "f"(acc[0]), "f"(acc[1]), "f"(acc[2]),
-                    "f"(acc[3]) : "memory");
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(out_slot<NT>(sbase, tile, buf, half, n, lane)), "f"(acc[n][0]), "f"(acc[n][1]),
+                        "f"(acc[n][2]), "f"(acc[n][3]) : "memory");
     warp_arrive(B.out_full(tile, buf), lane);
     return true;
 }
 
 // One consumer warp's steps of batch b: warp pair `slot` takes tile
 // slot >> lanes_log2 at chunk c + (slot & (lanes - 1)) of every step.
-template <int TYPE, int H>
+// xtoken[n] is the activation row this lane reads for column tile n.
+template <int TYPE, int H, int NT>
 __device__ bool consume_batch(const TcParams& P, const Barriers& B, const Walker& it, const uint8_t* smem,
-                              int slot, int lane, int xtoken, Ring& ring, float (&acc)[4],
-                              volatile uint32_t* abort_flag) {
+                              int slot, int lane, const int (&xtoken)[NT], Ring<Smem<NT>::kStages>& ring,
+                              float (&acc)[NT][4], volatile uint32_t* abort_flag) {
     const Batch& b = it.cur;
     constexpr int kPitch = TYPE == kPn3t ? kXPitchPn3t : kXPitchPn4t;
     const int j = slot >> b.lanes_log2;
@@ -473,15 +552,18 @@ __device__ bool consume_batch(const TcParams& P, const Barriers& B, const Walker
     const int cs = (j == 0 ? b.cs0 : 0) - q;             // work when cs <= c < ce
     const int ce = (j == b.nt - 1 ? b.ce_last : b.chunks) - q;
     const int toff = slot * kTileBytes;
-    const int xoff = kStageWBytes + q * x_block_bytes(P.M, kPitch) + xtoken * kPitch;
+    const int xoff = kStageWBytes + q * x_block_bytes(P.M, kPitch);
     for (int c = it.cstart; c < it.cend; c += b.lanes) {
         if (!warp_wait(B.full(ring.s), ring.phase, P.timeout_ns, abort_flag, lane)) {
             if (lane == 0) raise_timeout(P, abort_flag);
             return false;
         }
         if (in && c >= cs && c < ce) {
-            const uint8_t* stage = smem + ring.s * kStageBytes;
-            mma_tile_half<TYPE, H>(stage + toff, stage + xoff, lane, acc);
+            const uint8_t* stage = smem + ring.s * Smem<NT>::kStageBytes;
+            const uint8_t* xrow[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) xrow[n] = stage + xoff + xtoken[n] * kPitch;
+            mma_tile_half<TYPE, H, NT>(stage + toff, xrow, lane, acc);
         }
         warp_arrive(B.empty(ring.s), lane);
         ring.advance();
@@ -489,16 +571,22 @@ __device__ bool consume_batch(const TcParams& P, const Barriers& B, const Walker
     return !*abort_flag;
 }
 
+// One CTA per SM.  Its 18 warps sit on the SM's four schedulers as 5, 5, 4,
+// 4, and a scheduler's 16,384 registers over 5 warps of 32 threads allow at
+// most 96 registers per thread (what the launch bounds give).
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ TcParams P) {
+    using L = Smem<NT>;
+    constexpr int kStages = L::kStages;
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     Barriers B;
-    B.full0 = sbase + kBarrierOffset;
+    B.full0 = sbase + L::kBarrierOffset;
     B.empty0 = B.full0 + kStages * 8;
     B.ofull0 = B.empty0 + kStages * 8;
     B.ofree0 = B.ofull0 + kBatchTiles * kOutBuffers * 8;
     volatile uint32_t* abort_flag =
-        reinterpret_cast<volatile uint32_t*>(smem + kBarrierOffset + kNumBarriers * 8);
+        reinterpret_cast<volatile uint32_t*>(smem + L::kBarrierOffset + L::kNumBarriers * 8);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // programmatic dependent launch: the next kernel may start now; this one
     // touches activations, outputs and the workspace only after the previous
@@ -548,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
                 }
         }
         griddep_wait();
-        Ring ring;
+        Ring<kStages> ring;
         int idx = 0;
         bool stop = false;
         while (!it.done && !stop) {
@@ -584,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
                     nbox = __popc(mask);
                 }
                 const uint32_t full = B.full(ring.s);
-                const uint32_t stage = sbase + ring.s * kStageBytes;
+                const uint32_t stage = sbase + ring.s * L::kStageBytes;
                 // a box past the last row or the end of x is zero-filled and still counts in full
                 if (lane == 0) mbar_arrive_expect_tx(full, nq * xtx + static_cast<uint32_t>(nbox * kTileBytes));
                 __syncwarp();
@@ -660,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
                 }
             }
             if (!ok) break;
-            flush_batch(P, cur, lane, sbase, bufs);
+            flush_batch<NT>(P, cur, lane, sbase, bufs);
 #pragma unroll
             for (int p = 0; p < kBatchTiles; ++p) {
                 if (p >= slots) continue;
@@ -674,23 +762,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         // ------------------------------------------------------- consumers --
         griddep_wait();
         const int slot = warp >> 1, half = warp & 1;
-        const int xtoken = (lane >> 2) < P.M ? (lane >> 2) : 0;
+        int xtoken[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) xtoken[n] = 8 * n + (lane >> 2) < P.M ? 8 * n + (lane >> 2) : 0;
         Walker it;
         it.init(P, u0, u1);
-        Ring ring;
+        Ring<kStages> ring;
         uint32_t handoffs = 0;
         while (!it.done) {
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float acc[NT][4];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
             bool ok;
             if (P.t[it.cur.e].type == kPn3t)
-                ok = half == 0 ? consume_batch<kPn3t, 0>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag)
-                               : consume_batch<kPn3t, 1>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag);
+                ok = half == 0
+                    ? consume_batch<kPn3t, 0, NT>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag)
+                    : consume_batch<kPn3t, 1, NT>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag);
             else
-                ok = half == 0 ? consume_batch<kPn4t, 0>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag)
-                               : consume_batch<kPn4t, 1>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag);
+                ok = half == 0
+                    ? consume_batch<kPn4t, 0, NT>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag)
+                    : consume_batch<kPn4t, 1, NT>(P, B, it, smem, slot, lane, xtoken, ring, acc, abort_flag);
             if (!ok) break;
             if (slot < it.cur.nt * it.cur.lanes &&
-                !handoff(P, B, sbase, slot, half, lane, handoffs++, acc, abort_flag))
+                !handoff<NT>(P, B, sbase, slot, half, lane, handoffs++, acc, abort_flag))
                 break;
             it.next_batch(P);
         }
@@ -775,6 +869,8 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* stat
     }
     P.count = count;
     P.M = M;
+    const int nt = M > 8 ? 2 : 1;                  // 8-column tiles
+    P.x_rows = 8 * nt;
     // every range spans at least one whole tile, so a tile has at most two owners
     uint64_t grid = units / static_cast<uint64_t>(max_chunks);
     if (grid > static_cast<uint64_t>(tc_max_ctas(num_sms))) grid = tc_max_ctas(num_sms);
@@ -788,23 +884,26 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* stat
     P.timeout_ns = timeout_ns;
     P.stall_first_step = stall;
 
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    static bool attr_set[2] = {false, false};   // per process; the attribute is per function
+    const int smem_bytes = nt == 1 ? Smem<1>::kBytes : Smem<2>::kBytes;
+    if (!attr_set[nt - 1]) {
+        cudaError_t e = nt == 1
+            ? cudaFuncSetAttribute(gemv_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
+            : cudaFuncSetAttribute(gemv_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[nt - 1] = true;
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(P.grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_tc_kernel, P);
+    return nt == 1 ? cudaLaunchKernelEx(&cfg, gemv_tc_kernel<1>, P) : cudaLaunchKernelEx(&cfg, gemv_tc_kernel<2>, P);
 }
 
 }  // namespace pn

@@ -4,9 +4,15 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/pn.h"
+
 namespace pn {
 
-constexpr int kMaxM = 8;
+// Records e as the CUDA error behind this thread's latest PN_ECUDA (see
+// pn_last_cuda_error), clears the runtime's last error and returns PN_ECUDA.
+pn_status cuda_error(cudaError_t e);
+
+constexpr int kMaxM = 16;
 constexpr int kMaxLayer = 8;
 
 // One tensor of a GEMV launch, as the host hands it to a kernel.

@@ -26,8 +26,8 @@
 
 namespace {
 
-// Room for the workspace of a device with up to 339 SMs (the workspace size
-// depends only on the SM count: about 1.5 KiB per SM).
+// Room for the workspace of a device with up to 203 SMs (the workspace size
+// depends only on the SM count: about 2.5 KiB per SM).
 constexpr size_t kNoAllocScratchBytes = 512 * 1024;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -39,15 +39,14 @@ void* g_scratch_ptr[kMaxDevices] = {};                 // device address per dev
 // The scratch array's device address on the current device (looked up once).
 pn_status scratch_address(void** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return PN_ECUDA; }
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return pn::cuda_error(e);
     if (dev < 0 || dev >= kMaxDevices) return PN_EUNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_scratch_ptr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return PN_ECUDA;
-        }
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return pn::cuda_error(e);
+        if (!p) return PN_ECUDA;
         g_scratch_ptr[dev] = p;
     }
     *out = g_scratch_ptr[dev];
@@ -72,15 +71,11 @@ extern "C" pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t
     // cleared before every launch.
     int sms = 0;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return PN_ECUDA;
-    }
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return pn::cuda_error(e);
     const pn::WorkspaceLayout L = pn::workspace_layout(sms);
-    if (cudaMemsetAsync(ws, 0, L.total, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
-        cudaGetLastError();
-        return PN_ECUDA;
-    }
+    if ((e = cudaMemsetAsync(ws, 0, L.total, reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return pn::cuda_error(e);
     return pn_gemv_ex(type, W, N, K, x, M, y, ws, kNoAllocScratchBytes, PN_ALGO_AUTO, stream);
 }

@@ -15,7 +15,7 @@ import torch
 PN3T = 124
 PN4T = 125
 ALGO_AUTO, ALGO_TENSOR_CORE, ALGO_CUDA_CORE = 0, 1, 2
-MAX_M = 8
+MAX_M = 16
 MAX_LAYER = 8
 STATUS = {0: "PN_OK", 1: "PN_EINVAL", 2: "PN_EALIGN", 3: "PN_EUNSUPPORTED", 4: "PN_ECUDA",
           5: "PN_ETIMEOUT"}
@@ -27,9 +27,11 @@ _lib = None
 
 
 class PnError(RuntimeError):
-    def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {STATUS.get(status, status)}")
+    def __init__(self, status: int, what: str, cuda_error: str | None = None):
+        detail = f" ({cuda_error})" if cuda_error else ""
+        super().__init__(f"{what}: {STATUS.get(status, status)}{detail}")
         self.status = status
+        self.cuda_error = cuda_error
 
 
 class _Desc(ctypes.Structure):
@@ -50,6 +52,8 @@ def lib() -> ctypes.CDLL:
             L.pn_abi_version.restype = i32
             L.pn_status_string.restype = ctypes.c_char_p
             L.pn_status_string.argtypes = [i32]
+            L.pn_last_cuda_error.restype = ctypes.c_char_p
+            L.pn_last_cuda_error.argtypes = []
             L.pn_weights_per_block.restype = i32
             L.pn_weights_per_block.argtypes = [i32]
             L.pn_row_bytes.restype = sz
@@ -84,7 +88,8 @@ def lib() -> ctypes.CDLL:
 
 def _check(status: int, what: str) -> None:
     if status != 0:
-        raise PnError(status, what)
+        cuda = lib().pn_last_cuda_error().decode() if status == 4 else None
+        raise PnError(status, what, cuda)
 
 
 def _stream(stream=None) -> int:
@@ -162,7 +167,7 @@ class Workspace:
 
 def gemv(pn_type: int, W: torch.Tensor, K: int, x: torch.Tensor, y: torch.Tensor | None = None,
          workspace: Workspace | None = None, algo: int = ALGO_AUTO, stream=None) -> torch.Tensor:
-    """y[M][N] = decode(W)[N][K] @ x[M][K]^T with fp32 accumulation (1 <= M <= 8)."""
+    """y[M][N] = decode(W)[N][K] @ x[M][K]^T with fp32 accumulation (1 <= M <= 16)."""
     _require(W, torch.uint8, "W")
     _require(x, torch.float16, "x")
     if x.dim() == 1:

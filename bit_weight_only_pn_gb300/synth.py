@@ -132,4 +132,6 @@ CONFIGS = {
     2: dict(name="pn4t N=5120 K=17408 M=1", tensors=((PN4T, 17408, 5120),), M=1),
     3: dict(name="27B-class layer, 7 tensors, M=1", tensors=LAYER_27B, M=1),
     4: dict(name="27B-class layer, 7 tensors, M=8", tensors=LAYER_27B, M=8),
+    # the M 9 .. 16 band: one token plus 15 drafts over the same layer
+    5: dict(name="27B-class layer, 7 tensors, M=16", tensors=LAYER_27B, M=16),
 }

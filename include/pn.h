@@ -76,7 +76,7 @@ typedef enum {
 } pn_algo;
 
 #define PN_BLOCK_BYTES 34
-#define PN_MAX_M 8            /* largest activation count M per GEMV */
+#define PN_MAX_M 16           /* largest activation count M per GEMV */
 #define PN_MAX_LAYER 8        /* most tensors per pn_gemv_layer call */
 
 /* Version of this ABI (incremented on any incompatible change). */
@@ -84,6 +84,11 @@ int pn_abi_version(void);
 
 /* Human-readable name of a status code (static string). */
 const char* pn_status_string(pn_status s);
+
+/* Name of the CUDA runtime error (as cudaGetErrorName gives it) behind the
+ * latest PN_ECUDA that a failing CUDA call caused on the calling host thread;
+ * "cudaSuccess" if there was none.  Static string. */
+const char* pn_last_cuda_error(void);
 
 /* Weights per block (80 / 64) or 0 for an unknown type. */
 int pn_weights_per_block(int type);
@@ -115,7 +120,7 @@ pn_status pn_unpack(int type, const void* W, int64_t N, int64_t K, float* w, pn_
  * them, which adds the other block's part in a fixed order, so results are
  * deterministic.  That needs device scratch: a status word and, per
  * thread-block boundary, hand-off slots and a counter.  The size depends only
- * on the device's SM count (about 1.5 KiB per SM), so calls of any shape can
+ * on the device's SM count (about 2.5 KiB per SM), so calls of any shape can
  * share one workspace.
  *
  * pn_workspace_bytes(total_rows): bytes needed by one call whose tensors have
@@ -132,10 +137,10 @@ pn_status pn_workspace_init(void* workspace, size_t workspace_bytes, pn_stream s
 pn_status pn_workspace_status(void* workspace, size_t workspace_bytes, pn_stream stream);
 
 /*
- * pn_gemv: y[m][r] = sum_k w[r][k] * x[m][k] for m < M (1 <= M <= 8), r < N,
+ * pn_gemv: y[m][r] = sum_k w[r][k] * x[m][k] for m < M (1 <= M <= 16), r < N,
  * where w is W decoded as in pn_unpack.  This is the decode GEMV of token
- * generation (M = 1) and its skinny verification batch (M <= 8, one token plus
- * drafts).  Products are exact in fp32 and sums are kept in fp32; every output
+ * generation (M = 1) and its skinny verification batch (M <= 16, one token
+ * plus up to 15 drafts); the weights cross memory once whatever M is.  Products are exact in fp32 and sums are kept in fp32; every output
  * is within 1e-5 * sum_k |w[r][k] x[m][k]| + 1e-6 of the exact value.
  * Alignment: W and x 16-byte aligned for the tensor-core kernel (otherwise
  * PN_ALGO_AUTO uses the CUDA-core kernel, which needs W and x 2-byte and y
@@ -181,7 +186,7 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
  *
  * Scratch: a fixed 512 KiB array in the library's device image, which every
  * GPU that loads the library holds until the process exits.  A device whose
- * workspace (pn_workspace_bytes) would not fit (more than 339 SMs) gets
+ * workspace (pn_workspace_bytes) would not fit (more than 203 SMs) gets
  * PN_EINVAL and nothing is launched.  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress, which may load the
  * library's device module); make that first call before capturing a stream

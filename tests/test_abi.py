@@ -58,7 +58,7 @@ def test_argument_checks_return_before_any_launch(lib):
     assert g(7, FAKE, 16, 5120, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
     assert g(124, FAKE, 16, 5121, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
     assert g(124, FAKE, 16, 5120, FAKE * 2, 0, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
-    assert g(124, FAKE, 16, 5120, FAKE * 2, 9, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
+    assert g(124, FAKE, 16, 5120, FAKE * 2, 17, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
     assert g(124, FAKE, -1, 5120, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL
     # null pointers, misaligned pointers
     assert g(124, None, 16, 5120, FAKE * 2, 1, FAKE * 4, FAKE * 8, 1 << 20, 0, None) == PN_EINVAL

@@ -108,11 +108,11 @@ def test_gemv_every_m(pn, dev, oracle, pn_type, algo):
     bpb = GEOMETRY[pn_type][0]
     for N, nb in SHAPES:
         K = nb * bpb
-        W, x8 = synth_case(oracle, pn_type, N, K, 8, 0x900 + N)
+        W, x16 = synth_case(oracle, pn_type, N, K, 16, 0x900 + N)
         Wd = to_dev(W, dev)
         ws = pn.Workspace(N, dev)
-        for M in range(1, 9):
-            x = x8[:M]
+        for M in range(1, 17):
+            x = x16[:M]
             y_ref, abs_sum = oracle.gemv(pn_type, W, K, x)
             y = pn.gemv(pn_type, Wd, K, to_dev(x, dev), workspace=ws, algo=a).cpu().numpy()
             assert ws.status() == 0
@@ -166,7 +166,7 @@ def test_gemv_extreme_values(pn, dev, oracle):
         N, K = 64, 8 * bpb
         w = synth.weights(0x12, N, K) * np.float32(2000.0)
         W = oracle.pack(pn_type, w)
-        x = np.full((8, K), 65504.0, dtype=np.float16)
+        x = np.full((16, K), 65504.0, dtype=np.float16)
         x[1::2] *= -1
         y_ref, abs_sum = oracle.gemv(pn_type, W, K, x)
         for a in (pn.ALGO_TENSOR_CORE, pn.ALGO_CUDA_CORE):
@@ -233,12 +233,12 @@ def big_inputs(oracle):
     return get
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 @pytest.mark.parametrize("cfg", [0, 1, 2])
 def test_gemv_full_size_sampled(pn, dev, oracle, big_inputs, cfg, M):
     from bit_weight_only_pn_gb300 import synth
     (pn_type, K, N), = synth.CONFIGS[cfg]["tensors"]
-    W, x = big_inputs(cfg, 0, pn_type, K, N, 8)
+    W, x = big_inputs(cfg, 0, pn_type, K, N, 16)
     x = x[:M]
     ws = pn.Workspace(N, dev)
     y = pn.gemv(pn_type, to_dev(W, dev), K, to_dev(x, dev), workspace=ws).cpu().numpy()
@@ -248,14 +248,14 @@ def test_gemv_full_size_sampled(pn, dev, oracle, big_inputs, cfg, M):
     assert_gemv_close(y[:, rows], y_ref, abs_sum)
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 def test_layer_full_size_sampled(pn, dev, oracle, big_inputs, M):
     from bit_weight_only_pn_gb300 import synth
-    cfg = 3 if M == 1 else 4
+    cfg = {1: 3, 8: 4, 16: 5}[M]
     entries, host = [], []
     total_rows = 0
     for e, (pn_type, K, N) in enumerate(synth.LAYER_27B):
-        W, x = big_inputs(3, e, pn_type, K, N, 8)
+        W, x = big_inputs(3, e, pn_type, K, N, 16)
         x = x[:M]
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
         entries.append((pn_type, to_dev(W, dev), K, to_dev(x, dev), y))
@@ -275,7 +275,7 @@ def test_layer_small_full_compare(pn, dev, oracle):
     shapes = [(PN3T, 640, 300), (PN4T, 512, 129), (PN3T, 1280, 1000), (PN4T, 1024, 16),
               (PN4T, 2048, 77)]
     for a in (pn.ALGO_AUTO, pn.ALGO_CUDA_CORE):
-        for M in (1, 3, 8):
+        for M in (1, 3, 8, 9, 16):
             entries, refs = [], []
             for i, (t, K, N) in enumerate(shapes):
                 W, x = synth_case(oracle, t, N, K, M, 0x700 + i)
