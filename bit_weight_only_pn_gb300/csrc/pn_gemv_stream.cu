@@ -28,8 +28,8 @@
 //
 // Work split.  A unit is a 15-row tile x one 8-block chunk (272 bytes per
 // row).  Units are numbered tile-major over every tensor of the call; the grid
-// splits them into equal contiguous ranges of at least one tile, and the
-// eight warps of a block split the block's range again.  A warp's whole tiles
+// splits them into equal contiguous ranges (see kCostPn3t), each at least one
+// tile long, and the eight warps of a block split the block's range again.  A warp's whole tiles
 // are stored directly; the parts of a tile split between warps are added in
 // warp order by the last warp to deliver (a shared-memory counter); for a tile
 // cut by a block boundary both blocks swap their tagged part into a shared
@@ -58,6 +58,12 @@ constexpr int kChunkBlocks = 8;
 constexpr int kChunkBytes = kChunkBlocks * kBlockBytes;   // 272
 constexpr int kBoxWords = kChunkBytes / 4;                // 68
 constexpr int kBoxBytes = kRows * kChunkBytes;            // 4080
+// Relative cost of one unit, pn3t / pn4t, for the split of the units over
+// the thread blocks.  This kernel's time follows its memory stream more than
+// its decode: on a mixed pn3t / pn4t layer an even split of the bytes measured
+// fastest (weighting pn3t units 1.07 to 1.25 times a pn4t unit was 3 to 7 %
+// slower), so both weigh the same.
+constexpr uint32_t kCostPn3t = 1, kCostPn4t = 1;
 constexpr int kStageBytes = 4096;
 constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 // The all-ones code rows (pn3t, pn4t) stand in for row 15 of every stage; they
@@ -98,7 +104,7 @@ struct SParams {
     int count;
     int M;
     int grid;
-    uint32_t units;                // units * grid < 2^32 (checked on the host)
+    CostSplit split;               // the blocks' unit ranges
     uint32_t* status;
     uint64_t* tagged;              // [boundary][kSlotFloats] {tag, value bits}
     uint64_t timeout_ns;
@@ -119,7 +125,7 @@ struct Cursor {
 };
 
 __device__ __forceinline__ uint32_t range_start(const SParams& P, int c) {
-    return P.units * static_cast<uint32_t>(c) / static_cast<uint32_t>(P.grid);
+    return P.split.start(c);
 }
 
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -792,13 +798,11 @@ cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* 
     }
     P.count = count;
     P.M = M;
+    if (units * kWarps >= (1ull << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
+    for (int e = 0; e < count; ++e)
+        P.split.add(static_cast<uint32_t>(P.t[e].chunks) * P.t[e].tiles, P.t[e].type == kPn3t ? kCostPn3t : kCostPn4t);
     // every block range spans at least one whole tile, so a tile has at most two blocks
-    uint64_t grid = units / static_cast<uint64_t>(max_chunks);
-    if (grid > static_cast<uint64_t>(stream_max_ctas(num_sms))) grid = stream_max_ctas(num_sms);
-    if (grid < 1) grid = 1;
-    if (units * grid >= (1ull << 32) || units * kWarps >= (1ull << 32)) return cudaErrorInvalidValue;
-    P.grid = static_cast<int>(grid);
-    P.units = static_cast<uint32_t>(units);
+    P.grid = P.split.fit_grid(stream_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
     P.status = status;
     P.tagged = tagged;
     P.timeout_ns = timeout_ns;

@@ -14,9 +14,10 @@
 //  * Work unit = one 16-row tile x one 8-block chunk (8 x 34 = 272 bytes per
 //    row, 16-byte aligned whenever the row is).  Units are numbered tile-major
 //    over every tensor of the call and the persistent grid (at most one CTA per
-//    SM, each range at least one tile long) splits them into equal contiguous
-//    ranges, so every SM streams the same number of bytes and only a CTA's
-//    first and last tile can be shared, each with one neighbour.
+//    SM, each range at least one tile long) splits them into contiguous
+//    ranges of equal decode cost (a pn3t unit weighs more than a pn4t one), so
+//    every SM finishes at about the same time and only a CTA's first and last
+//    tile can be shared, each with one neighbour.
 //  * A CTA walks its tiles in batches of up to 8 consecutive tiles of one
 //    tensor, chunk by chunk (one step = one chunk of the batch's tiles, so the
 //    activation chunk is staged once for 8 tiles), last batch first so that
@@ -74,6 +75,12 @@ constexpr int kOutBuffers = 2;
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                  // PN_ETIMEOUT
 constexpr int kSlotFloats = kTileRows * kMaxM;          // 256: one tile's partial sums
+// Relative cost of one unit, pn3t / pn4t, for the split of the units over
+// the thread blocks (5 / 4 MMAs per block and column tile and their code
+// pairs, plus the per-block work both share).  Measured on a mixed pn3t / pn4t
+// layer at 8 and 16 tokens, 16 / 15 was about 4 % faster than an even split
+// of the units; larger ratios (8 / 7 and up) were slower again.
+constexpr uint32_t kCostPn3t = 16, kCostPn4t = 15;
 
 // Shared-memory layout of the kernel with NT 8-column tiles (M <= 8 NT).
 template <int NT>
@@ -98,6 +105,7 @@ struct Smem {
 };
 
 static_assert(kStageWBytes % 128 == 0, "TMA destinations stay aligned");
+static_assert(kSplitMax == kMaxLayer, "the work split holds every tensor of a call");
 static_assert(2 * 8 <= kMaxM, "partial-sum slots hold 16 tokens");
 
 // Bytes between the activation blocks of consecutive chunk lanes.
@@ -128,7 +136,7 @@ struct TcParams {
     int M;
     int x_rows;                    // activation rows a stage holds (8 per column tile)
     int grid;
-    uint32_t units;                // units * grid < 2^32 (checked on the host)
+    CostSplit split;               // the blocks' unit ranges
     uint32_t* status;
     uint32_t* counters;            // one per CTA boundary
     float* partials;               // [boundary][side][kSlotFloats]
@@ -159,7 +167,7 @@ __device__ __forceinline__ bool slot_work(const Batch& b, int c, int p, int& j, 
 
 // First unit of CTA c's range.
 __device__ __forceinline__ uint32_t range_start(const TcParams& P, int c) {
-    return P.units * static_cast<uint32_t>(c) / static_cast<uint32_t>(P.grid);
+    return P.split.start(c);
 }
 
 // Tensor, tile and chunk of unit u.
@@ -871,13 +879,11 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* stat
     P.M = M;
     const int nt = M > 8 ? 2 : 1;                  // 8-column tiles
     P.x_rows = 8 * nt;
+    if (units >= (1ull << 32)) return cudaErrorInvalidValue;   // 32-bit unit numbers
+    for (int e = 0; e < count; ++e)
+        P.split.add(static_cast<uint32_t>(P.t[e].chunks) * P.t[e].tiles, P.t[e].type == kPn3t ? kCostPn3t : kCostPn4t);
     // every range spans at least one whole tile, so a tile has at most two owners
-    uint64_t grid = units / static_cast<uint64_t>(max_chunks);
-    if (grid > static_cast<uint64_t>(tc_max_ctas(num_sms))) grid = tc_max_ctas(num_sms);
-    if (grid < 1) grid = 1;
-    if (units * grid >= (1ull << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
-    P.grid = static_cast<int>(grid);
-    P.units = static_cast<uint32_t>(units);
+    P.grid = P.split.fit_grid(tc_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
     P.status = status;
     P.counters = counters;
     P.partials = partials;
