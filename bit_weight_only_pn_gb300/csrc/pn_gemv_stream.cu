@@ -64,6 +64,7 @@ constexpr int kBoxBytes = kRows * kChunkBytes;            // 4080
 // fastest (weighting pn3t units 1.07 to 1.25 times a pn4t unit was 3 to 7 %
 // slower), so both weigh the same.
 constexpr uint32_t kCostPn3t = 1, kCostPn4t = 1;
+constexpr int kMaxGrid = 512;                             // thread blocks per launch, at most
 constexpr int kStageBytes = 4096;
 constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 // The all-ones code rows (pn3t, pn4t) stand in for row 15 of every stage; they
@@ -104,7 +105,7 @@ struct SParams {
     int count;
     int M;
     int grid;
-    CostSplit split;               // the blocks' unit ranges
+    uint32_t starts[kMaxGrid + 1]; // block c's units are [starts[c], starts[c + 1])
     uint32_t* status;
     uint64_t* tagged;              // [boundary][kSlotFloats] {tag, value bits}
     uint64_t timeout_ns;
@@ -125,7 +126,7 @@ struct Cursor {
 };
 
 __device__ __forceinline__ uint32_t range_start(const SParams& P, int c) {
-    return P.split.start(c);
+    return P.starts[c];
 }
 
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -770,7 +771,7 @@ cudaError_t launch_bpm(const SParams& P, cudaStream_t s) {
 
 }  // namespace
 
-int stream_max_ctas(int num_sms) { return 2 * num_sms; }
+int stream_max_ctas(int num_sms) { return 2 * num_sms < kMaxGrid ? 2 * num_sms : kMaxGrid; }
 
 size_t stream_tagged_bytes(int num_sms) {
     return static_cast<size_t>(stream_max_ctas(num_sms) + 1) * kSlotFloats * sizeof(uint64_t);
@@ -799,10 +800,12 @@ cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* 
     P.count = count;
     P.M = M;
     if (units * kWarps >= (1ull << 32)) return cudaErrorInvalidValue;   // 32-bit unit arithmetic
+    CostSplit split{};
     for (int e = 0; e < count; ++e)
-        P.split.add(static_cast<uint32_t>(P.t[e].chunks) * P.t[e].tiles, P.t[e].type == kPn3t ? kCostPn3t : kCostPn4t);
+        split.add(static_cast<uint32_t>(P.t[e].chunks) * P.t[e].tiles, P.t[e].type == kPn3t ? kCostPn3t : kCostPn4t);
     // every block range spans at least one whole tile, so a tile has at most two blocks
-    P.grid = P.split.fit_grid(stream_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
+    P.grid = split.fit_grid(stream_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
+    for (int c = 0; c <= P.grid; ++c) P.starts[c] = split.start(c);
     P.status = status;
     P.tagged = tagged;
     P.timeout_ns = timeout_ns;

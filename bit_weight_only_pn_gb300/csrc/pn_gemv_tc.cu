@@ -81,6 +81,7 @@ constexpr int kSlotFloats = kTileRows * kMaxM;          // 256: one tile's parti
 // layer at 8 and 16 tokens, 16 / 15 was about 4 % faster than an even split
 // of the units; larger ratios (8 / 7 and up) were slower again.
 constexpr uint32_t kCostPn3t = 16, kCostPn4t = 15;
+constexpr int kMaxGrid = 256;                           // thread blocks per launch, at most
 
 // Shared-memory layout of the kernel with NT 8-column tiles (M <= 8 NT).
 template <int NT>
@@ -105,7 +106,6 @@ struct Smem {
 };
 
 static_assert(kStageWBytes % 128 == 0, "TMA destinations stay aligned");
-static_assert(kSplitMax == kMaxLayer, "the work split holds every tensor of a call");
 static_assert(2 * 8 <= kMaxM, "partial-sum slots hold 16 tokens");
 
 // Bytes between the activation blocks of consecutive chunk lanes.
@@ -136,7 +136,7 @@ struct TcParams {
     int M;
     int x_rows;                    // activation rows a stage holds (8 per column tile)
     int grid;
-    CostSplit split;               // the blocks' unit ranges
+    uint32_t starts[kMaxGrid + 1]; // block c's units are [starts[c], starts[c + 1])
     uint32_t* status;
     uint32_t* counters;            // one per CTA boundary
     float* partials;               // [boundary][side][kSlotFloats]
@@ -167,7 +167,7 @@ __device__ __forceinline__ bool slot_work(const Batch& b, int c, int p, int& j, 
 
 // First unit of CTA c's range.
 __device__ __forceinline__ uint32_t range_start(const TcParams& P, int c) {
-    return P.split.start(c);
+    return P.starts[c];
 }
 
 // Tensor, tile and chunk of unit u.
@@ -851,7 +851,7 @@ bool encode_x(CUtensorMap* map, const GemvTensor& t, int M) {
 
 }  // namespace
 
-int tc_max_ctas(int num_sms) { return num_sms; }
+int tc_max_ctas(int num_sms) { return num_sms < kMaxGrid ? num_sms : kMaxGrid; }
 
 size_t tc_partial_bytes(int num_sms) {
     return static_cast<size_t>(tc_max_ctas(num_sms) + 1) * 2 * kSlotFloats * sizeof(float);
@@ -880,10 +880,12 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* stat
     const int nt = M > 8 ? 2 : 1;                  // 8-column tiles
     P.x_rows = 8 * nt;
     if (units >= (1ull << 32)) return cudaErrorInvalidValue;   // 32-bit unit numbers
+    CostSplit split{};
     for (int e = 0; e < count; ++e)
-        P.split.add(static_cast<uint32_t>(P.t[e].chunks) * P.t[e].tiles, P.t[e].type == kPn3t ? kCostPn3t : kCostPn4t);
+        split.add(static_cast<uint32_t>(P.t[e].chunks) * P.t[e].tiles, P.t[e].type == kPn3t ? kCostPn3t : kCostPn4t);
     // every range spans at least one whole tile, so a tile has at most two owners
-    P.grid = P.split.fit_grid(tc_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
+    P.grid = split.fit_grid(tc_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
+    for (int c = 0; c <= P.grid; ++c) P.starts[c] = split.start(c);
     P.status = status;
     P.counters = counters;
     P.partials = partials;

@@ -15,6 +15,63 @@ pn_status cuda_error(cudaError_t e);
 constexpr int kMaxM = 16;
 constexpr int kMaxLayer = 8;
 
+// ---------------------------------------------------------- work split --
+// The GEMV kernels number a call's work units (row tile x 8-block chunk)
+// tensor by tensor and give every thread block one contiguous range.  Units
+// of different tensors cost different decode work (a pn3t block-row holds 80
+// codes, a pn4t one 64), so the ranges split the call's total cost, not its
+// unit count, evenly: tensor e's units are [base[e], base[e+1]) at w[e] each,
+// and block c's range starts at the first unit whose cumulative cost reaches
+// total * c / grid.  With one weight for every tensor this is the plain even
+// split of the units.  Computed on the host; the kernels read each block's
+// first unit from a table in their parameters.
+struct CostSplit {
+    uint32_t base[kMaxLayer + 1];      // base[count] = all units
+    uint64_t cbase[kMaxLayer + 1];     // cost of the units before tensor e; cbase[count] = total
+    uint32_t w[kMaxLayer];             // cost of one unit of tensor e (>= 1)
+    int count;
+    int grid;
+
+    // First unit of block c's range; start(grid) is the end of the last one.
+    // Non-decreasing in c.
+    uint32_t start(int c) const {
+        if (c >= grid) return base[count];
+        const uint64_t target = cbase[count] * static_cast<uint64_t>(c) / static_cast<uint64_t>(grid);
+        int e = 0;
+        while (e + 1 < count && cbase[e + 1] <= target) ++e;
+        const uint64_t u = base[e] + (target - cbase[e] + w[e] - 1) / w[e];
+        return u < base[e + 1] ? static_cast<uint32_t>(u) : base[e + 1];
+    }
+
+    // Tensor e has `units` units at cost `cost` each (in call order).
+    void add(uint32_t units, uint32_t cost) {
+        w[count] = cost;
+        base[count + 1] = base[count] + units;
+        cbase[count + 1] = cbase[count] + static_cast<uint64_t>(units) * cost;
+        ++count;
+    }
+
+    // The largest grid <= max_grid whose ranges all hold at least
+    // min_units units (so a tile of at most min_units units has at most two
+    // owners); at least 1.
+    int fit_grid(int max_grid, uint32_t min_units) {
+        const uint32_t units = base[count];
+        int g = static_cast<int>(units / (min_units > 0 ? min_units : 1));
+        g = g < max_grid ? g : max_grid;
+        for (grid = g < 1 ? 1 : g; grid > 1; --grid) {
+            bool ok = true;
+            uint32_t prev = 0;
+            for (int c = 1; c <= grid && ok; ++c) {
+                const uint32_t next = start(c);
+                ok = next - prev >= min_units;
+                prev = next;
+            }
+            if (ok) break;
+        }
+        return grid;
+    }
+};
+
 // One tensor of a GEMV launch, as the host hands it to a kernel.
 struct GemvTensor {
     const uint8_t* W;       // PN rows, row stride nb * 34 bytes
