@@ -9,7 +9,8 @@ numpy arrays.
 Source: tensorless docs, "Why a P100-native weight format" (block layout,
 half-word packing, exact decode, mid-tread codes with a signed scale; the
 runtime Hadamard rotation of the activations, section "How Qwen3.8-27B-PN3
-uses it").
+uses it"); tensorless docs, "What the fork adds", and the v100-skinny README,
+"How QPN works" (prefill: weights rebuilt transiently, then a GEMM).
 """
 from __future__ import annotations
 
@@ -72,6 +73,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_float_to_half.argtypes = [ctypes.c_float]
     lib.oracle_hadamard.restype = ctypes.c_int
     lib.oracle_hadamard.argtypes = [c_void_p, ctypes.c_int, i64, ctypes.c_int, c_void_p, c_void_p]
+    lib.oracle_unpack_f16.restype = ctypes.c_int
+    lib.oracle_unpack_f16.argtypes = [ctypes.c_int, c_void_p, i64, i64, c_void_p]
+    lib.oracle_gemm_f16.restype = ctypes.c_int
+    lib.oracle_gemm_f16.argtypes = [c_void_p, i64, i64, c_void_p, ctypes.c_int, c_void_p, c_void_p]
     return lib
 
 
@@ -175,6 +180,36 @@ class Oracle:
         if rc:
             raise ValueError(f"oracle_hadamard failed ({rc})")
         return (out, o32) if want_f32 else out
+
+    def unpack_f16(self, pn_type: int, W: np.ndarray, K: int) -> np.ndarray:
+        """PN bytes [N][row_bytes] -> fp16 weights [N][K], each the exact
+        decode rounded once to fp16 (reading R11, prefill reconstruction)."""
+        W = np.ascontiguousarray(W, dtype=np.uint8)
+        N = W.shape[0]
+        if W.shape[1] != self.row_bytes(pn_type, K):
+            raise ValueError("row size does not match K")
+        w16 = np.empty((N, K), dtype=np.float16)
+        rc = self.lib.oracle_unpack_f16(pn_type, W.ctypes.data, N, K, w16.view(np.uint16).ctypes.data)
+        if rc:
+            raise ValueError(f"oracle_unpack_f16 failed ({rc})")
+        return w16
+
+    def gemm_f16(self, w16: np.ndarray, x: np.ndarray, want_abs: bool = True):
+        """y[M][N] = x w16^T in fp64, rounded to fp32; also sum |w x| if asked."""
+        w16 = np.ascontiguousarray(w16, dtype=np.float16)
+        x = np.ascontiguousarray(x, dtype=np.float16)
+        if x.ndim == 1:
+            x = x[None, :]
+        (N, K), M = w16.shape, x.shape[0]
+        if x.shape[1] != K:
+            raise ValueError("shape mismatch")
+        y = np.empty((M, N), dtype=np.float32)
+        a = np.empty((M, N), dtype=np.float64) if want_abs else None
+        rc = self.lib.oracle_gemm_f16(w16.view(np.uint16).ctypes.data, N, K, x.view(np.uint16).ctypes.data,
+                                      M, y.ctypes.data, a.ctypes.data if want_abs else None)
+        if rc:
+            raise ValueError(f"oracle_gemm_f16 failed ({rc})")
+        return (y, a) if want_abs else y
 
     def half_to_float(self, h: int) -> float:
         return float(self.lib.oracle_half_to_float(h))

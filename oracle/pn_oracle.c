@@ -321,3 +321,59 @@ int oracle_hadamard(const uint16_t* x, int M, int64_t K, int B, uint16_t* out, f
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------ prefill, large M --- */
+
+/*
+ * Prefill reconstruction (tensorless docs, "What the fork adds": the engine
+ * dequantizes the weights for prefill and runs a chunked GEMM; v100-skinny
+ * README, "How QPN works": above the skinny band the weights are rebuilt
+ * transiently from the packed codes and never kept).  The pages give no
+ * precision for the rebuilt weights.  Reading R11: each weight is the exact
+ * fp32 product d * (n - z) of the decode, rounded once to fp16 (nearest, ties
+ * to even; a product beyond the fp16 range becomes +-inf).
+ *
+ * W: PN rows [N][row_bytes]; w16: fp16 bit patterns [N][K].
+ */
+int oracle_unpack_f16(int type, const uint8_t* W, int64_t N, int64_t K, uint16_t* w16)
+{
+    oracle_fmt f;
+    if (!oracle_format(type, &f) || N < 0 || K <= 0 || K % f.per_block || (N > 0 && (!W || !w16)))
+        return ORACLE_EINVAL;
+    int64_t nb = K / f.per_block;
+    float wblk[80];
+    for (int64_t r = 0; r < N; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            decode_block(&f, W + (r * nb + b) * ORACLE_BLOCK_BYTES, wblk);
+            for (int k = 0; k < f.per_block; ++k)
+                w16[r * K + b * f.per_block + k] = oracle_float_to_half(wblk[k]);
+        }
+    return ORACLE_OK;
+}
+
+/*
+ * The GEMM of the rebuilt weights: y[m][n] = sum_k w16[n][k] * x[m][k] for
+ * m < M, n < N, every product and sum in fp64 and rounded to fp32 once at the
+ * end; abs_sum (if not NULL) receives sum_k |w16[n][k] * x[m][k]| in fp64.
+ * w16 [N][K] and x [M][K] are fp16 bit patterns; y and abs_sum are [M][N].
+ */
+int oracle_gemm_f16(const uint16_t* w16, int64_t N, int64_t K, const uint16_t* x, int M,
+                    float* y, double* abs_sum)
+{
+    if (N < 0 || K <= 0 || M < 1 || (N > 0 && (!w16 || !x || !y))) return ORACLE_EINVAL;
+    for (int m = 0; m < M; ++m) {
+        const uint16_t* xrow = x + (int64_t)m * K;
+        for (int64_t n = 0; n < N; ++n) {
+            const uint16_t* wrow = w16 + n * K;
+            double sum = 0.0, sum_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = (double)oracle_half_to_float(wrow[k]) * (double)oracle_half_to_float(xrow[k]);
+                sum += p;
+                sum_abs += fabs(p);
+            }
+            y[(int64_t)m * N + n] = (float)sum;
+            if (abs_sum) abs_sum[(int64_t)m * N + n] = sum_abs;
+        }
+    }
+    return ORACLE_OK;
+}

@@ -366,10 +366,101 @@ def pin_hadamard_structure(o):
         assert np.all(np.abs(back - x.astype(np.float64)) <= 2.0 ** -9 * np.abs(x).max() * 4)
 
 
+def _uniform_block(pn_type, dbits, j):
+    """One block whose every code is n = j + z, with scale bits dbits."""
+    bpb, cpw, bits, z = GEOMETRY[pn_type]
+    word = _replicate(j + z, bits, cpw // 2)
+    return np.frombuffer(_block_bytes(dbits, [word] * 8), dtype=np.uint8)[None, :]
+
+
+def pin_unpack_f16_worked(o):
+    # Hand-derived fp16 roundings of the exact product d*(n - z) (reading R11):
+    # (1 + 2^-10)*3 = 3 + 3*2^-10 is halfway between two fp16 values and goes up
+    # to the even one, (1 + 3*2^-10)*3 is halfway and goes down to the even one,
+    # (1 + 2^-10)*7 rounds up, products on the fp16 grid stay exact, 65504*2
+    # overflows to inf, 2^-24*3 is the subnormal 3*2^-24, and -d*0 is -0.
+    cases = [(PN3T, 0x3C01, 3, 0x4202), (PN3T, 0x3C03, 3, 0x4204), (PN3T, 0x3C01, -3, 0xC202),
+             (PN3T, 0x3C01, 2, 0x4001), (PN3T, 0x3C01, -4, 0xC401), (PN4T, 0x3C01, 7, 0x4702),
+             (PN4T, 0x7BFF, 1, 0x7BFF), (PN4T, 0x7BFF, 2, 0x7C00), (PN3T, 0x7BFF, -4, 0xFC00),
+             (PN3T, 0x0001, 3, 0x0003), (PN3T, 0xBC01, 0, 0x8000), (PN4T, 0x3C00, -8, 0xC800)]
+    for t, dbits, j, want in cases:
+        bpb = GEOMETRY[t][0]
+        got = o.unpack_f16(t, _uniform_block(t, dbits, j), bpb)
+        assert np.all(got.view(np.uint16) == want), (t, hex(dbits), j)
+
+
+def pin_unpack_f16_is_rounded_decode(o):
+    # Each reconstructed weight is numpy's fp16 rounding (an independent IEEE
+    # implementation) of the pinned exact decode, for scales across the whole
+    # fp16 range, every code, and several blocks and rows.
+    rng = np.random.default_rng(29)
+    for t in TYPES:
+        bpb, cpw, bits, z = GEOMETRY[t]
+        nb, N = 3, 40
+        W = np.zeros((N, nb * 34), dtype=np.uint8)
+        for r in range(N):
+            for b in range(nb):
+                dbits = int(rng.integers(0, 0x7C00)) | (int(rng.integers(0, 2)) << 15)
+                words = [int(v) for v in rng.integers(0, 2 ** 32, size=8, dtype=np.uint64)]
+                W[r, b * 34:(b + 1) * 34] = np.frombuffer(_block_bytes(dbits, words), dtype=np.uint8)
+        with np.errstate(over="ignore"):
+            want = o.unpack(t, W, nb * bpb).astype(np.float16)
+        got = o.unpack_f16(t, W, nb * bpb)
+        assert np.array_equal(got.view(np.uint16), want.view(np.uint16)), t
+
+
+def pin_gemm_f16_exact_tiny(o):
+    # Brute force with exact rationals: the oracle's GEMM is the fp32 rounding
+    # of sum_k w[n][k] x[m][k]; rows, tokens and the abs sum checked one by one.
+    rng = np.random.default_rng(31)
+    N, K, M = 3, 24, 4
+    w = (0.05 * rng.standard_normal((N, K))).astype(np.float16)
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    y, a = o.gemm_f16(w, x)
+    assert y.shape == (M, N)
+    for m in range(M):
+        for n in range(N):
+            terms = [Fraction(float(w[n, k])) * Fraction(float(x[m, k])) for k in range(K)]
+            exact = sum(terms, Fraction(0))
+            absx = sum((abs(p) for p in terms), Fraction(0))
+            tol = Fraction(K, 2 ** 52) * absx + Fraction(abs(float(np.spacing(np.float32(float(exact))))))
+            assert abs(Fraction(float(y[m, n])) - exact) <= tol
+            assert abs(Fraction(float(a[m, n])) - absx) <= Fraction(K, 2 ** 52) * absx
+
+
+def pin_gemm_f16_matches_gemv_on_grid(o):
+    # Scales with a 7-bit mantissa times steps of at most 3 bits need at most
+    # 11 significant bits, so those weights are exact in fp16: the GEMM of the
+    # reconstructed weights must then equal the (pinned) PN GEMV bit for bit,
+    # and a one-hot x returns a column of the reconstructed weights.
+    rng = np.random.default_rng(37)
+    for t in TYPES:
+        bpb, _, _, z = GEOMETRY[t]
+        nb, N, M = 5, 21, 6
+        d = (rng.choice([-1.0, 1.0], size=(N, nb)) * (1.0 + 8 * rng.integers(0, 128, size=(N, nb)) / 1024.0)
+             * np.exp2(rng.integers(-9, -5, size=(N, nb)).astype(np.float64)))
+        q = rng.integers(-z, z, size=(N, nb * bpb))
+        q[:, ::bpb] = -z                                  # one full-range step per block
+        w = (np.repeat(d, bpb, axis=1) * q).astype(np.float32)
+        assert np.array_equal(w.astype(np.float16).astype(np.float32), w)
+        W = o.pack(t, w)
+        assert np.array_equal(o.unpack(t, W, nb * bpb), w)
+        x = rng.standard_normal((M, nb * bpb)).astype(np.float16)
+        w16 = o.unpack_f16(t, W, nb * bpb)
+        assert np.array_equal(w16.astype(np.float32), w)
+        assert np.array_equal(o.gemm_f16(w16, x, want_abs=False), o.gemv(t, W, nb * bpb, x, want_abs=False))
+        k = int(rng.integers(0, nb * bpb))
+        e = np.zeros((1, nb * bpb), dtype=np.float16)
+        e[0, k] = 1.0
+        assert np.array_equal(o.gemm_f16(w16, e, want_abs=False)[0], w[:, k])
+
+
 ALL_PINS = [pin_block_geometry, pin_worked_blocks, pin_fp16_conversion, pin_decode_exact_all_scales,
             pin_half_structure, pin_every_half_round_trips, pin_full_range_and_bound,
             pin_on_grid_lossless, pin_special_blocks, pin_gemv_exact_tiny, pin_gemv_independent,
-            pin_hadamard_worked, pin_hadamard_dense, pin_hadamard_structure]
+            pin_hadamard_worked, pin_hadamard_dense, pin_hadamard_structure,
+            pin_unpack_f16_worked, pin_unpack_f16_is_rounded_decode, pin_gemm_f16_exact_tiny,
+            pin_gemm_f16_matches_gemv_on_grid]
 
 
 # ------------------------------------------------------------------- tests ----
@@ -426,6 +517,14 @@ MUTATIONS = {
     "hadamard_odd_scale": ("if (m % 2) s = ldexpf(sqrt2, -(m + 1) / 2);", "if (m % 2) s = ldexpf(1.0f, -(m + 1) / 2);"),
     "hadamard_block_offset": ("const int64_t off = (int64_t)row * K + base;", "const int64_t off = (int64_t)row * K;"),
     "hadamard_partner": ("const float a = v[i], b = v[i + h];", "const float a = v[i], b = v[(i + h) % B];\n                    if (h > 1) continue;"),
+    "f16_block_offset": ("w16[r * K + b * f.per_block + k] = oracle_float_to_half(wblk[k]);",
+                         "w16[r * K + k] = oracle_float_to_half(wblk[k]);"),
+    "f16_scale_rounded_first": ("w16[r * K + b * f.per_block + k] = oracle_float_to_half(wblk[k]);",
+                                "w16[r * K + b * f.per_block + k] = oracle_float_to_half(wblk[k] + wblk[k] * 0x1p-12f);"),
+    "gemm_transposed_weights": ("double p = (double)oracle_half_to_float(wrow[k]) * (double)oracle_half_to_float(xrow[k]);",
+                                "double p = (double)oracle_half_to_float(w16[k * N + n]) * (double)oracle_half_to_float(xrow[k]);"),
+    "gemm_fp32_accumulate": ("double sum = 0.0, sum_abs = 0.0;", "float sum = 0.0f; double sum_abs = 0.0;"),
+    "gemm_token_zero": ("const uint16_t* xrow = x + (int64_t)m * K;", "const uint16_t* xrow = x;"),
 }
 
 
