@@ -132,6 +132,26 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
     return PN_OK;
 }
 
+// Checks shared by pn_gemm_f16 and pn_prefill (w16 is the fp16 operand: the
+// caller's matrix or the scratch chunk).
+pn_status check_gemm(int64_t N, int64_t K, const void* x, int64_t M, const float* y, int64_t ldy,
+                     void* workspace, size_t workspace_bytes, int* major) {
+    if (N < 0 || K <= 0 || K % 8 != 0 || K > INT32_MAX || M < 1 || M > INT32_MAX || ldy < N) return PN_EINVAL;
+    if (N > 65535LL * 128) return PN_EINVAL;
+    if (N == 0) return PN_OK;
+    if (!x || !y || !workspace) return PN_EINVAL;
+    if (!aligned(x, 16) || !aligned(y, 4)) return PN_EALIGN;
+    if (!aligned(workspace, 256)) return PN_EINVAL;
+    int sms = 0;
+    pn_status st = device_info(&sms, major);
+    if (st != PN_OK) return st;
+    if (*major < 10) return PN_EUNSUPPORTED;
+    if (pn::workspace_layout(sms).total > workspace_bytes) return PN_EINVAL;
+    const size_t ybytes = (static_cast<size_t>(M - 1) * ldy + N) * 4;
+    if (overlaps(y, ybytes, x, static_cast<size_t>(M) * K * 2)) return PN_EINVAL;
+    return PN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -262,6 +282,68 @@ pn_status pn_hadamard(const uint16_t* x, int M, int64_t K, int block, uint16_t* 
     if (K / block > INT32_MAX) return PN_EINVAL;
     const cudaError_t e = pn::launch_hadamard(x, M, K, block, out, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
+}
+
+pn_status pn_unpack_f16(int type, const void* W, int64_t N, int64_t K, uint16_t* w16, pn_stream stream) {
+    const int bpb = per_block(type);
+    if (bpb == 0 || K <= 0 || K % bpb != 0 || N < 0) return PN_EINVAL;
+    if (N == 0) return PN_OK;
+    if (!W || !w16) return PN_EINVAL;
+    if (!aligned(W, 2) || !aligned(w16, 4)) return PN_EALIGN;
+    if (overlaps(w16, static_cast<size_t>(N) * K * 2, W, static_cast<size_t>(N) * (K / bpb) * PN_BLOCK_BYTES))
+        return PN_EINVAL;
+    const cudaError_t e = pn::launch_unpack_f16(type, W, N, K / bpb, w16, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
+}
+
+pn_status pn_gemm_f16(const uint16_t* w16, int64_t N, int64_t K, const uint16_t* x, int64_t M, float* y,
+                      int64_t ldy, void* workspace, size_t workspace_bytes, pn_stream stream) {
+    int major = 0;
+    pn_status st = check_gemm(N, K, x, M, y, ldy, workspace, workspace_bytes, &major);
+    if (st != PN_OK || N == 0) return st;
+    if (!w16) return PN_EINVAL;
+    if (!aligned(w16, 16)) return PN_EALIGN;
+    const size_t ybytes = (static_cast<size_t>(M - 1) * ldy + N) * 4;
+    if (overlaps(y, ybytes, w16, static_cast<size_t>(N) * K * 2)) return PN_EINVAL;
+    uint32_t* status = static_cast<uint32_t*>(workspace);
+    const cudaError_t e = pn::launch_gemm_f16(w16, N, K, x, M, y, ldy, status, g_timeout_ns.load(),
+                                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
+}
+
+pn_status pn_prefill(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t M, float* y,
+                     void* scratch, size_t scratch_bytes, void* workspace, size_t workspace_bytes,
+                     pn_stream stream) {
+    const int bpb = per_block(type);
+    if (bpb == 0 || K <= 0 || K % bpb != 0) return PN_EINVAL;
+    int major = 0;
+    pn_status st = check_gemm(N, K, x, M, y, N, workspace, workspace_bytes, &major);
+    if (st != PN_OK || N == 0) return st;
+    if (!W || !scratch) return PN_EINVAL;
+    if (!aligned(W, 2) || !aligned(scratch, 16)) return PN_EALIGN;
+    const int tile = pn::gemm_f16_tile_rows();
+    int64_t chunk = static_cast<int64_t>(scratch_bytes / (static_cast<size_t>(K) * 2)) / tile * tile;
+    if (chunk < tile) return PN_EINVAL;
+    if (chunk > N) chunk = N;
+    const size_t wbytes = static_cast<size_t>(N) * (K / bpb) * PN_BLOCK_BYTES;
+    const size_t ybytes = static_cast<size_t>(M) * N * 4;
+    const size_t sbytes = static_cast<size_t>(chunk) * K * 2;
+    if (overlaps(y, ybytes, W, wbytes) || overlaps(scratch, sbytes, W, wbytes) ||
+        overlaps(scratch, sbytes, x, static_cast<size_t>(M) * K * 2) || overlaps(scratch, sbytes, y, ybytes))
+        return PN_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t* w16 = static_cast<uint16_t*>(scratch);
+    uint32_t* status = static_cast<uint32_t*>(workspace);
+    const int64_t nb = K / bpb;
+    const size_t row_bytes = static_cast<size_t>(nb) * PN_BLOCK_BYTES;
+    for (int64_t r0 = 0; r0 < N; r0 += chunk) {
+        const int64_t rows = N - r0 < chunk ? N - r0 : chunk;
+        cudaError_t e = pn::launch_unpack_f16(type, static_cast<const uint8_t*>(W) + r0 * row_bytes, rows, nb, w16, s);
+        if (e == cudaSuccess)
+            e = pn::launch_gemm_f16(w16, rows, K, x, M, y + r0, N, status, g_timeout_ns.load(), s);
+        if (e != cudaSuccess) return pn::cuda_error(e);
+    }
+    return PN_OK;
 }
 
 const char* pn_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }

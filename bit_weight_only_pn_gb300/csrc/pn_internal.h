@@ -89,6 +89,15 @@ cudaError_t launch_hadamard(const uint16_t* x, int M, int64_t K, int block, uint
 cudaError_t launch_unpack(int type, const void* W, int64_t N, int64_t nb, float* w, cudaStream_t s);
 cudaError_t launch_pack(int type, const float* w, int64_t N, int64_t nb, void* W, cudaStream_t s);
 
+// Prefill: PN rows -> fp16 (exact decode rounded once), and the fp16 GEMM
+// y[m * ldy + r] = sum_k w16[r][k] x[m][k] on the tcgen05 tensor cores (w16,
+// x 16-byte aligned, K a multiple of 8; rows a multiple of
+// gemm_f16_tile_rows() except the last chunk).
+cudaError_t launch_unpack_f16(int type, const void* W, int64_t N, int64_t nb, uint16_t* w16, cudaStream_t s);
+cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const uint16_t* x, int64_t M,
+                            float* y, int64_t ldy, uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
+int gemm_f16_tile_rows();
+
 // CUDA-core GEMV: any nb, W and x 2-byte aligned, y 4-byte aligned.
 cudaError_t launch_gemv_simt(const GemvTensor& t, int M, cudaStream_t s);
 

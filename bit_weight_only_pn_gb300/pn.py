@@ -76,6 +76,12 @@ def lib() -> ctypes.CDLL:
             L.pn_gemv_layer.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, vp]
             L.pn_gemv_layer_ex.restype = i32
             L.pn_gemv_layer_ex.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, i32, vp]
+            L.pn_unpack_f16.restype = i32
+            L.pn_unpack_f16.argtypes = [i32, vp, i64, i64, vp, vp]
+            L.pn_gemm_f16.restype = i32
+            L.pn_gemm_f16.argtypes = [vp, i64, i64, vp, i64, vp, i64, vp, sz, vp]
+            L.pn_prefill.restype = i32
+            L.pn_prefill.argtypes = [i32, vp, i64, i64, vp, i64, vp, vp, sz, vp, sz, vp]
             L.pn_hadamard.restype = i32
             L.pn_hadamard.argtypes = [vp, i32, i64, i32, vp, vp]
             L.pn_set_wait_timeout_ns.restype = None
@@ -214,6 +220,59 @@ def hadamard(x: torch.Tensor, block: int, out: torch.Tensor | None = None, strea
     _require(out, torch.float16, "out")
     _check(lib().pn_hadamard(_ptr(x), M, K, block, _ptr(out), _stream(stream)), "pn_hadamard")
     return out
+
+
+def unpack_f16(pn_type: int, W: torch.Tensor, K: int, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """PN rows uint8 [N][row_bytes] -> fp16 weights [N][K] (exact decode, one rounding)."""
+    _require(W, torch.uint8, "W")
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float16, device=W.device)
+    _require(out, torch.float16, "out")
+    _check(lib().pn_unpack_f16(pn_type, _ptr(W), N, K, _ptr(out), _stream(stream)), "pn_unpack_f16")
+    return out
+
+
+def gemm_f16(w16: torch.Tensor, x: torch.Tensor, y: torch.Tensor | None = None,
+             workspace: Workspace | None = None, stream=None) -> torch.Tensor:
+    """y[M][N] = x[M][K] @ w16[N][K]^T, fp16 products, fp32 accumulation (tcgen05)."""
+    _require(w16, torch.float16, "w16")
+    _require(x, torch.float16, "x")
+    N, K = w16.shape
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=w16.device)
+    _require(y, torch.float32, "y")
+    if workspace is None:
+        workspace = Workspace(N, w16.device)
+    _check(lib().pn_gemm_f16(_ptr(w16), N, K, _ptr(x), M, _ptr(y), y.shape[1], workspace.ptr,
+                             workspace.nbytes, _stream(stream)), "pn_gemm_f16")
+    return y
+
+
+def prefill(pn_type: int, W: torch.Tensor, K: int, x: torch.Tensor, y: torch.Tensor | None = None,
+            scratch: torch.Tensor | None = None, workspace: Workspace | None = None,
+            stream=None) -> torch.Tensor:
+    """y[M][N] for large M: PN rows rebuilt as fp16 chunk by chunk into
+    ``scratch`` (default: room for every row), then the fp16 GEMM."""
+    _require(W, torch.uint8, "W")
+    _require(x, torch.float16, "x")
+    N = W.shape[0]
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=W.device)
+    _require(y, torch.float32, "y")
+    if scratch is None:
+        rows = max(128, (N + 127) // 128 * 128)
+        scratch = torch.empty(rows * K, dtype=torch.float16, device=W.device)
+    _require(scratch, torch.float16, "scratch")
+    if workspace is None:
+        workspace = Workspace(N, W.device)
+    _check(lib().pn_prefill(pn_type, _ptr(W), N, K, _ptr(x), M, _ptr(y), _ptr(scratch),
+                            scratch.numel() * 2, workspace.ptr, workspace.nbytes, _stream(stream)),
+           "pn_prefill")
+    return y
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -221,6 +221,41 @@ pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const u
 pn_status pn_hadamard(const uint16_t* x, int M, int64_t K, int block, uint16_t* out, pn_stream stream);
 
 /*
+ * Prefill (large M).  The pages' engine dequantizes the weights for prefill
+ * and runs a chunked GEMM, rebuilding weights transiently from the packed
+ * codes without keeping them (tensorless docs, "What the fork adds";
+ * v100-skinny README, "How QPN works").  Reading taken here: each rebuilt
+ * weight is the exact decode d * (n - z) rounded once to fp16 (nearest, ties
+ * to even; beyond the fp16 range +-inf), and the GEMM multiplies fp16 by fp16
+ * exactly and accumulates in fp32 (on the tcgen05 tensor cores).
+ *
+ * pn_unpack_f16: PN rows W [N][row_bytes] -> fp16 w16 [N][K] as above.  W
+ * 2-byte and w16 4-byte aligned; they must not overlap.
+ *
+ * pn_gemm_f16: y[m * ldy + r] = sum_k w16[r][k] * x[m][k] for r < N, m < M
+ * (w16 fp16 [N][K], x fp16 [M][K], y fp32 rows of ldy >= N floats).  w16 and
+ * x 16-byte aligned, K a positive multiple of 8, y 4-byte aligned and not
+ * overlapping w16 or x; 1 <= M < 2^31, N <= 8,388,480.  The workspace is the
+ * GEMV's (pn_workspace_bytes); only its status word is used, which records
+ * PN_ETIMEOUT if a device-side wait gives up (read with pn_workspace_status).
+ * Each output sums its K products in fp32 in K order, 16 at a time; it is
+ * within (K/16 + 16) * 2^-24 * sum_k |w16 x| + 1e-6 of the exact sum.
+ *
+ * pn_prefill: the whole path, y[m][r] = sum_k w16[r][k] x[m][k] for the PN
+ * tensor W [N][row_bytes]: the rows are rebuilt chunk by chunk into `scratch`
+ * (fp16, caller-owned, 16-byte aligned; a chunk is the largest multiple of
+ * 128 rows that fits, at least 128 rows = 256 K bytes) and multiplied by x;
+ * y is fp32 [M][N].  Same alignment rules as pn_gemm_f16; all launches are
+ * asynchronous on `stream`, in order, so scratch is reused safely.
+ */
+pn_status pn_unpack_f16(int type, const void* W, int64_t N, int64_t K, uint16_t* w16, pn_stream stream);
+pn_status pn_gemm_f16(const uint16_t* w16, int64_t N, int64_t K, const uint16_t* x, int64_t M, float* y,
+                      int64_t ldy, void* workspace, size_t workspace_bytes, pn_stream stream);
+pn_status pn_prefill(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int64_t M, float* y,
+                     void* scratch, size_t scratch_bytes, void* workspace, size_t workspace_bytes,
+                     pn_stream stream);
+
+/*
  * Testing aid: the time limit, in nanoseconds, of every device-side wait in
  * the tensor-core kernel (default 1e9).  A wait that runs out stops its thread
  * block, which records PN_ETIMEOUT in the workspace status word and returns

@@ -105,3 +105,23 @@ def test_hadamard_checks(lib):
     assert h(None, 1, 96, 32, FAKE * 2, None) == PN_EINVAL
     assert h(FAKE + 1, 1, 96, 32, FAKE * 2, None) == PN_EALIGN
     assert h(FAKE, 1, 96, 32, FAKE + 64, None) == PN_EINVAL
+
+
+def test_prefill_checks(lib):
+    # checks that come before any device query or launch
+    u, g, p = lib.pn_unpack_f16, lib.pn_gemm_f16, lib.pn_prefill
+    assert u(7, FAKE, 4, 80, FAKE * 2, None) == PN_EINVAL                  # unknown type
+    assert u(124, FAKE, 4, 81, FAKE * 2, None) == PN_EINVAL                # K not whole blocks
+    assert u(124, FAKE, 4, 80, FAKE * 2 + 2, None) == PN_EALIGN            # w16 not 4-byte aligned
+    assert u(125, FAKE, 4, 64, FAKE + 16, None) == PN_EINVAL               # w16 overlaps W
+    assert u(124, FAKE, 0, 80, FAKE * 2, None) == 0                        # nothing to do
+    ws = FAKE * 8
+    assert g(FAKE, 16, 100, FAKE * 2, 4, FAKE * 4, 16, ws, 1 << 20, None) == PN_EINVAL   # K % 8
+    assert g(FAKE, 16, 128, FAKE * 2, 4, FAKE * 4, 15, ws, 1 << 20, None) == PN_EINVAL   # ldy < N
+    assert g(FAKE, 16, 128, FAKE * 2, 0, FAKE * 4, 16, ws, 1 << 20, None) == PN_EINVAL   # M = 0
+    assert g(FAKE, 16, 128, FAKE * 2 + 8, 4, FAKE * 4, 16, ws, 1 << 20, None) == PN_EALIGN   # x
+    assert g(FAKE, 16, 128, FAKE * 2, 4, FAKE * 4 + 2, 16, ws, 1 << 20, None) == PN_EALIGN   # y
+    assert g(FAKE, 16, 128, FAKE * 2, 4, FAKE * 4, 16, ws + 16, 1 << 20, None) == PN_EINVAL  # workspace
+    assert g(FAKE, 0, 128, FAKE * 2, 4, FAKE * 4, 16, ws, 1 << 20, None) == 0
+    assert p(124, FAKE, 16, 100, FAKE * 2, 4, FAKE * 4, FAKE * 16, 1 << 20, ws, 1 << 20, None) == PN_EINVAL
+    assert p(125, FAKE, 16, 128, FAKE * 2, 0, FAKE * 4, FAKE * 16, 1 << 20, ws, 1 << 20, None) == PN_EINVAL
