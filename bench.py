@@ -5,8 +5,10 @@ Workload (default): pn3t GEMV, N = 17408 rows, K = 5120 (64 blocks of 34 bytes
 per row, 37,879,808 bytes of packed weights), M = 1, fp16 x, fp32 y -- the
 FFN gate/up shape of a 27B-class model at the tensorless pages' widths.  A
 step is one GEMV over one batch (one token's x).  Other workloads:
-``--config 0|2|3|4`` (3/4: one decoder layer's seven GEMVs in one fused call at
-M = 1 / M = 8).
+``--config 0|2|3|4|5`` (3/4/5: one decoder layer's seven GEMVs in one fused
+call at M = 1 / 8 / 16) and ``--config 6``, the prefill path (a 4096-token
+prompt through the pn3t 5120->17408 tensor: fp16 rebuild + tcgen05 GEMM,
+reported in TFLOP/s against the tensor-core roofline).
 
 Timing: weights are resident in HBM; eight copies (more than twice the 129 MB
 L2) are rotated so every step reads its weights from HBM.  Steps are captured
@@ -54,7 +56,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4, 5, 6])
     ap.add_argument("--algo", choices=["auto", "tc", "cuda_core"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -325,6 +327,168 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, world, rank, local):
+    """The prefill path (config 6): one pn_prefill call per step -- the PN
+    rows rebuilt as fp16 into a scratch buffer holding the whole tensor, then
+    the tcgen05 GEMM with M tokens.  value = GEMM flops (2 M N K) per second."""
+    import torch
+    from bit_weight_only_pn_gb300 import build, pn, synth
+    if rank == 0 or not os.path.exists(pn.LIBRARY):
+        build.build()
+    dist_barrier(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name, tensors, M = workload(args.config)
+    (t, K, N), = tensors
+    steps = min(args.steps, 200)              # a step is ~0.5 ms: 200 keep the timed region short
+    warmup = min(max(args.warmup, 3), 20)
+    flops = 2.0 * M * N * K
+    w = torch.from_numpy(synth.weights(synth.weight_seed(args.config, 0), N, K)).to(dev)
+    W = pn.pack(t, w)
+    del w
+    x = torch.from_numpy(synth.activations(synth.x_seed(args.config, 0), M, K)).to(dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    scratch = torch.empty(N * K, dtype=torch.float16, device=dev)
+    ws = pn.Workspace(N, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        dist_barrier(world)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        dist_barrier(world)
+        return dist_max(world, a.elapsed_time(b)) / n
+
+    step = lambda: pn.prefill(t, W, K, x, y=y, scratch=scratch, workspace=ws, stream=stream)
+    props = torch.cuda.get_device_properties(local)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    clocks.start()
+    time.sleep(0.3)
+    clocks.mark()
+    ms_per_step = timed(step, steps)
+    clocks.mark()
+    clock_info = clocks.stop()
+    if ws.status(stream) != 0:
+        raise RuntimeError("device-side error in the timed region")
+    # the two kernels of a step, each timed alone on the same buffers
+    w16 = scratch.view(N, K)
+    ms_gemm = timed(lambda: pn.gemm_f16(w16, x, y=y, workspace=ws, stream=stream), steps)
+    ms_unpack = timed(lambda: pn.unpack_f16(t, W, K, out=w16, stream=stream), steps)
+    value = world * flops / (ms_per_step / 1e3) / 1e12
+
+    e2e = None
+    if args.e2e_steps > 0:
+        xh = torch.from_numpy(synth.activations(synth.x_seed(args.config, 0) + 1000, M, K)).pin_memory()
+        yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            x.copy_(xh, non_blocking=True)
+            step()
+            yh.copy_(y, non_blocking=True)
+            stream.synchronize()
+
+        n_e2e = min(args.e2e_steps, 20)
+        e_ms = timed(e2e_step, n_e2e)
+        e2e = {"value": world * flops / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": yh.numel() * 4,
+               "us_per_step": e_ms * 1e3, "steps": n_e2e,
+               "path": "pinned x -> device, pn_prefill via the Python binding, y -> pinned host, "
+                       "stream synchronised each step; PN weights resident"}
+
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            peak = float(json.load(fh)["bf16_tflops"])
+        peak_src = "measured cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops); fp16 runs at the bf16 rate"
+    except (OSError, KeyError, ValueError):
+        peak, peak_src = 1900.0, "fallback 1.9 PFLOP/s bf16 burst"
+    achieved = flops / (ms_gemm / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                "kernel": "gemm_f16_kernel", "kernel_ms": ms_gemm}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, desc, used = oracle_prefill_rate(t, K, N, M, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": used, "kind": "oracle", "sample": desc}
+    if rank != 0:
+        return
+    line = {
+        "metric": "PN prefill TFLOP/s (fp16 rebuild + tcgen05 GEMM)", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 products, f32 accumulate", "data": "synthetic",
+        "config": {"workload": name, "M": M, "tensors": [f"pn3t {K}->{N}"],
+                   "scratch": f"fp16, all {N} rows ({N * K * 2 / 1e6:.0f} MB), one chunk",
+                   "l2": "working set (PN rows, fp16 rows, x, y: 540 MB) larger than L2",
+                   "launch": "direct launches, two per step (rebuild, GEMM)",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "ms_gemm": ms_gemm, "ms_unpack_f16": ms_unpack,
+        "gpu_launches": 2 * steps,
+        "roofline": roofline,
+        "clocks": clock_info,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def oracle_prefill_rate(t, K, N, M, seconds):
+    """The CPU oracle's prefill (fp16 rebuild + fp64 GEMM) on a sample of
+    rows and tokens, repeated for about `seconds`; returns (TFLOP/s of the
+    GEMM's 2 M N K, description, threads)."""
+    import oracle
+    from bit_weight_only_pn_gb300 import synth
+    o = oracle.Oracle()
+    rows, toks = 64, 64
+    W = o.pack(t, synth.weight_rows(synth.weight_seed(9, 0), N, K, range(rows)))
+    x = synth.activations(synth.x_seed(9, 0), toks, K)
+    s = time.perf_counter()
+    o.gemm_f16(o.unpack_f16(t, W, K), x, want_abs=False)
+    first = time.perf_counter() - s
+    passes = max(1, int(round(seconds / max(first, 1e-6))))
+    s = time.perf_counter()
+    for _ in range(passes):
+        o.gemm_f16(o.unpack_f16(t, W, K), x, want_abs=False)
+    dt = time.perf_counter() - s
+    return (2.0 * rows * toks * K * passes / dt / 1e12,
+            f"{rows}/{N} rows x {toks}/{M} tokens, {passes} passes in {dt:.1f} s on 1 thread", 1)
+
+
+def run_reference_prefill(args, world, rank):
+    """The CPU oracle as the reference arm of the prefill workload (rank 0):
+    each step rebuilds and multiplies a fixed sample of rows and tokens."""
+    if rank != 0:
+        return
+    from bit_weight_only_pn_gb300 import synth
+    name, tensors, M = workload(args.config)
+    (t, K, N), = tensors
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    rate, desc, used = oracle_prefill_rate(t, K, N, M, per_step)
+    line = {
+        "impl": "reference", "metric": "PN prefill TFLOP/s (fp16 rebuild + tcgen05 GEMM)", "value": rate,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 2.0 * M * N * K / (rate * 1e12) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "M": M, "oracle": "plain C, fp64 accumulation"},
+        "cpu_baseline": {"value": rate, "unit": "TFLOP/s", "cores": used, "kind": "oracle", "sample": desc},
+        "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, world, rank, local):
     import torch
     from bit_weight_only_pn_gb300 import build, pn, synth
@@ -512,8 +676,12 @@ def run_ours(args, world, rank, local):
 def main():
     args = parse_args()
     world, rank, local = dist_setup(args)
+    from bit_weight_only_pn_gb300 import synth
+    prefill = synth.CONFIGS[args.config].get("prefill", False)
     if args.impl == "reference":
-        run_reference(args, world, rank)
+        run_reference_prefill(args, world, rank) if prefill else run_reference(args, world, rank)
+    elif prefill:
+        run_prefill(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

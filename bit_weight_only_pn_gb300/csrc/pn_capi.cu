@@ -135,18 +135,17 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
 // Checks shared by pn_gemm_f16 and pn_prefill (w16 is the fp16 operand: the
 // caller's matrix or the scratch chunk).
 pn_status check_gemm(int64_t N, int64_t K, const void* x, int64_t M, const float* y, int64_t ldy,
-                     void* workspace, size_t workspace_bytes, int* major) {
+                     void* workspace, size_t workspace_bytes, int* sms, int* major) {
     if (N < 0 || K <= 0 || K % 8 != 0 || K > INT32_MAX || M < 1 || M > INT32_MAX || ldy < N) return PN_EINVAL;
     if (N > 65535LL * 128) return PN_EINVAL;
     if (N == 0) return PN_OK;
     if (!x || !y || !workspace) return PN_EINVAL;
     if (!aligned(x, 16) || !aligned(y, 4)) return PN_EALIGN;
     if (!aligned(workspace, 256)) return PN_EINVAL;
-    int sms = 0;
-    pn_status st = device_info(&sms, major);
+    pn_status st = device_info(sms, major);
     if (st != PN_OK) return st;
     if (*major < 10) return PN_EUNSUPPORTED;
-    if (pn::workspace_layout(sms).total > workspace_bytes) return PN_EINVAL;
+    if (pn::workspace_layout(*sms).total > workspace_bytes) return PN_EINVAL;
     const size_t ybytes = (static_cast<size_t>(M - 1) * ldy + N) * 4;
     if (overlaps(y, ybytes, x, static_cast<size_t>(M) * K * 2)) return PN_EINVAL;
     return PN_OK;
@@ -298,15 +297,15 @@ pn_status pn_unpack_f16(int type, const void* W, int64_t N, int64_t K, uint16_t*
 
 pn_status pn_gemm_f16(const uint16_t* w16, int64_t N, int64_t K, const uint16_t* x, int64_t M, float* y,
                       int64_t ldy, void* workspace, size_t workspace_bytes, pn_stream stream) {
-    int major = 0;
-    pn_status st = check_gemm(N, K, x, M, y, ldy, workspace, workspace_bytes, &major);
+    int sms = 0, major = 0;
+    pn_status st = check_gemm(N, K, x, M, y, ldy, workspace, workspace_bytes, &sms, &major);
     if (st != PN_OK || N == 0) return st;
     if (!w16) return PN_EINVAL;
     if (!aligned(w16, 16)) return PN_EALIGN;
     const size_t ybytes = (static_cast<size_t>(M - 1) * ldy + N) * 4;
     if (overlaps(y, ybytes, w16, static_cast<size_t>(N) * K * 2)) return PN_EINVAL;
     uint32_t* status = static_cast<uint32_t*>(workspace);
-    const cudaError_t e = pn::launch_gemm_f16(w16, N, K, x, M, y, ldy, status, g_timeout_ns.load(),
+    const cudaError_t e = pn::launch_gemm_f16(w16, N, K, x, M, y, ldy, status, sms, g_timeout_ns.load(),
                                               reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
 }
@@ -316,8 +315,8 @@ pn_status pn_prefill(int type, const void* W, int64_t N, int64_t K, const uint16
                      pn_stream stream) {
     const int bpb = per_block(type);
     if (bpb == 0 || K <= 0 || K % bpb != 0) return PN_EINVAL;
-    int major = 0;
-    pn_status st = check_gemm(N, K, x, M, y, N, workspace, workspace_bytes, &major);
+    int sms = 0, major = 0;
+    pn_status st = check_gemm(N, K, x, M, y, N, workspace, workspace_bytes, &sms, &major);
     if (st != PN_OK || N == 0) return st;
     if (!W || !scratch) return PN_EINVAL;
     if (!aligned(W, 2) || !aligned(scratch, 16)) return PN_EALIGN;
@@ -340,7 +339,7 @@ pn_status pn_prefill(int type, const void* W, int64_t N, int64_t K, const uint16
         const int64_t rows = N - r0 < chunk ? N - r0 : chunk;
         cudaError_t e = pn::launch_unpack_f16(type, static_cast<const uint8_t*>(W) + r0 * row_bytes, rows, nb, w16, s);
         if (e == cudaSuccess)
-            e = pn::launch_gemm_f16(w16, rows, K, x, M, y + r0, N, status, g_timeout_ns.load(), s);
+            e = pn::launch_gemm_f16(w16, rows, K, x, M, y + r0, N, status, sms, g_timeout_ns.load(), s);
         if (e != cudaSuccess) return pn::cuda_error(e);
     }
     return PN_OK;

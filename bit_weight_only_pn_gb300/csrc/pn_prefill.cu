@@ -12,16 +12,16 @@
 //  * unpack_f16_kernel: one thread per code word, exact fp32 product, one
 //    rounding to fp16, half2 stores.  Memory-bound; it runs once per chunk of
 //    rows, so at prefill sizes it is a small fraction of the GEMM.
-//  * gemm_f16_kernel: one 128-row x 256-token output tile per CTA.  Warp 0
-//    lane 0 streams 64-wide K slices of the weight and activation tiles into
-//    a 4-stage shared-memory ring with 2-D TMA (128-byte swizzle, the layout
-//    the MMA reads directly); warp 1 lane 0 issues tcgen05.mma (kind::f16,
-//    M = 128, N = 256, K = 16, fp32 accumulator in 256 TMEM columns) and
-//    hands each stage back with tcgen05.commit; after the last slice all four
-//    warps read their 32 TMEM lanes (one weight row per thread) with
-//    tcgen05.ld and store y.  Consecutive CTAs share the weight tile and walk
-//    the token tiles, so the rebuilt weights cross HBM once and the
-//    activations are re-read from L2.
+//  * gemm_f16_kernel: persistent, one CTA per SM, output tiles of 128 rows x
+//    256 tokens taken round-robin (token tile fastest, so the CTAs working at
+//    one time share few weight tiles and the rebuilt weights cross HBM about
+//    once).  Warp 0 lane 0 streams 64-wide K slices of the weight and
+//    activation tiles into a 4-stage shared-memory ring with 2-D TMA
+//    (128-byte swizzle, the layout the MMA reads directly); warp 1 lane 0
+//    issues tcgen05.mma (kind::f16, M = 128, N = 256, K = 16) into one of two
+//    fp32 accumulators of 256 TMEM columns each and hands every stage back
+//    with tcgen05.commit; warps 2-5 read a finished accumulator (one weight
+//    row per thread, tcgen05.ld) and store y while the MMAs fill the other.
 //  * Every mbarrier wait is bounded in time; a CTA that gives up records
 //    PN_ETIMEOUT, lets its copies and MMAs in flight finish (bounded), frees
 //    its TMEM and returns.
@@ -73,17 +73,18 @@ constexpr int kTileTokens = 256;                     // tokens per tile (MMA N)
 constexpr int kKStep = 64;                           // K per stage: one 128-byte row of fp16
 constexpr int kMmaK = 16;                            // K per tcgen05.mma, kind::f16
 constexpr int kStages = 4;
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;                        // producer, MMA issuer, 4 epilogue warps
+constexpr int kAccBufs = 2;                          // TMEM accumulators (epilogue overlaps MMAs)
 constexpr int kABytes = kTileRows * kKStep * 2;      // 16384
 constexpr int kBBytes = kTileTokens * kKStep * 2;    // 32768
 constexpr int kStageBytes = kABytes + kBBytes;       // 49152
 constexpr int kBarOffset = kStages * kStageBytes;    // 196608
-constexpr int kNumBars = 2 * kStages + 1;            // full, empty, accumulator done
+constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;   // ring full / empty, accumulator full / empty, drain
 constexpr int kTmemSlot = kBarOffset + kNumBars * 8; // TMEM base address written by tcgen05.alloc
 constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kSmemUsed = kAbortSlot + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;         // slack to align the ring to 1024 bytes
-constexpr uint32_t kTmemCols = kTileTokens;          // fp32 accumulator: 128 lanes x 256 columns
+constexpr uint32_t kTmemCols = kAccBufs * kTileTokens;   // two fp32 accumulators of 128 lanes x 256 columns
 constexpr uint32_t kStatusTimeout = 5;               // PN_ETIMEOUT
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 
@@ -165,6 +166,8 @@ struct GemmParams {
     int rows;
     int M;
     int K;
+    int tiles_tok;             // ceil(M / 256)
+    int tiles;                 // tiles_tok * ceil(rows / 128)
     uint32_t* status;
     uint64_t timeout_ns;
 };
@@ -198,11 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
     const uint32_t bar0 = base + kBarOffset;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-    const uint32_t done = bar0 + 8u * (2 * kStages);
+    auto acc_full = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+    auto acc_empty = [&](int a) { return bar0 + 8u * (2 * kStages + kAccBufs + a); };
+    const uint32_t drain = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
     volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(smem + kAbortSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tok0 = blockIdx.x * kTileTokens;
-    const int row0 = blockIdx.y * kTileRows;
     const int nk = (P.K + kKStep - 1) / kKStep;
 
     if (threadIdx.x == 0) {
@@ -210,13 +213,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
-        mbar_init(done, 1);
+        for (int a = 0; a < kAccBufs; ++a) {
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), 4);       // one arrival per epilogue warp
+        }
+        mbar_init(drain, 1);
         *abort = 0u;
         fence_mbar_init();
         prefetch_tensormap(&P.amap);
         prefetch_tensormap(&P.bmap);
     }
-    if (warp == 0) {                      // the whole warp allocates the accumulator
+    if (warp == 0) {                          // the whole warp allocates the accumulators
         tmem_alloc(base + kTmemSlot, kTmemCols);
         tmem_relinquish();
     }
@@ -225,81 +232,116 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
-    if (warp == 0 && lane == 0) {
-        // ---------------------------------------------------------- producer --
-        int issued = 0;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            if (kb >= kStages &&
-                !wait_phase(empty(s), static_cast<uint32_t>((kb / kStages) - 1) & 1u, P.timeout_ns, abort, false)) {
-                raise_abort(P, abort);
-                break;
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------ producer --
+            int it = 0;                       // K slices issued, over all tiles
+            bool stop = false;
+            for (int t = blockIdx.x; t < P.tiles && !stop; t += gridDim.x) {
+                const int tok0 = (t % P.tiles_tok) * kTileTokens;
+                const int row0 = (t / P.tiles_tok) * kTileRows;
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int s = it % kStages;
+                    if (it >= kStages &&
+                        !wait_phase(empty(s), static_cast<uint32_t>((it / kStages) - 1) & 1u, P.timeout_ns, abort,
+                                    false)) {
+                        raise_abort(P, abort);
+                        stop = true;
+                        break;
+                    }
+                    if (*abort) { stop = true; break; }
+                    const uint32_t a = base + s * kStageBytes;
+                    mbar_arrive_expect_tx(full(s), kStageBytes);
+                    tma_load_2d(a, &P.amap, kb * kKStep, row0, full(s));
+                    tma_load_2d(a + kABytes, &P.bmap, kb * kKStep, tok0, full(s));
+                    ++it;
+                }
             }
-            if (*abort) break;
-            const uint32_t a = base + s * kStageBytes;
-            mbar_arrive_expect_tx(full(s), kStageBytes);
-            tma_load_2d(a, &P.amap, kb * kKStep, row0, full(s));
-            tma_load_2d(a + kABytes, &P.bmap, kb * kKStep, tok0, full(s));
-            ++issued;
+            // every copy this thread started lands before the CTA can exit:
+            // stage s was last filled by the largest issue i < it with i %
+            // kStages == s (after a normal run the MMA thread waited for all)
+            for (int s = 0; s < kStages; ++s) {
+                if (it <= s) continue;
+                const int last = s + kStages * ((it - 1 - s) / kStages);
+                wait_phase(full(s), static_cast<uint32_t>(last / kStages) & 1u, kDrainLimitNs, nullptr, false);
+            }
         }
-        // every copy this thread started lands before the CTA can exit: stage
-        // s was last filled by the largest issue i < issued with i % kStages
-        // == s (after a normal run the MMA thread has waited for all of them)
-        for (int s = 0; s < kStages; ++s) {
-            if (issued <= s) continue;
-            const int last = s + kStages * ((issued - 1 - s) / kStages);
-            wait_phase(full(s), static_cast<uint32_t>(last / kStages) & 1u, kDrainLimitNs, nullptr, false);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ----------------------------------------------------- MMA issue --
+            int it = 0, local = 0;
+            bool stop = false;
+            for (int t = blockIdx.x; t < P.tiles && !stop; t += gridDim.x, ++local) {
+                const int acc = local & 1;
+                // the epilogue has emptied this accumulator's previous tile
+                if (local >= kAccBufs &&
+                    !wait_phase(acc_empty(acc), static_cast<uint32_t>((local >> 1) + 1) & 1u, P.timeout_ns, abort,
+                                false)) {
+                    raise_abort(P, abort);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kTileTokens);
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int s = it % kStages;
+                    if (!wait_phase(full(s), static_cast<uint32_t>(it / kStages) & 1u, P.timeout_ns, abort, false)) {
+                        raise_abort(P, abort);
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a = base + s * kStageBytes;
+                    const uint32_t b = a + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kKStep / kMmaK; ++kk)
+                        mma_f16(d, smem_desc_sw128(a + kk * kMmaK * 2), smem_desc_sw128(b + kk * kMmaK * 2),
+                                (kb | kk) != 0 ? 1u : 0u);
+                    mma_commit(empty(s));     // the stage is free once these MMAs have read it
+                    ++it;
+                }
+                if (!stop) mma_commit(acc_full(acc));
+            }
+            mma_commit(drain);                // every MMA of this CTA finished (also after an abort)
         }
-    } else if (warp == 1 && lane == 0) {
-        // --------------------------------------------------------- MMA issue --
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            if (!wait_phase(full(s), static_cast<uint32_t>(kb / kStages) & 1u, P.timeout_ns, abort, false)) {
-                raise_abort(P, abort);
+    } else {
+        // --------------------------------------------------------- epilogue --
+        const int q = warp & 3;               // TMEM lane quadrant this warp may read
+        int local = 0;
+        for (int t = blockIdx.x; t < P.tiles; t += gridDim.x, ++local) {
+            const int acc = local & 1;
+            bool ok = true;
+            if (lane == 0)
+                ok = wait_phase(acc_full(acc), static_cast<uint32_t>(local >> 1) & 1u, P.timeout_ns, abort, true);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) {
+                if (lane == 0) raise_abort(P, abort);
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t a = base + s * kStageBytes;
-            const uint32_t b = a + kABytes;
+            const int tok0 = (t % P.tiles_tok) * kTileTokens;
+            const int row = (t / P.tiles_tok) * kTileRows + q * 32 + lane;
+            const uint32_t taddr = tmem + static_cast<uint32_t>(acc * kTileTokens) + (static_cast<uint32_t>(q * 32) << 16);
+            for (int c = 0; c < kTileTokens; c += 32) {
+                if (tok0 + c >= P.M) break;   // warp-uniform
+                uint32_t v[32];
+                tmem_ld32(taddr + static_cast<uint32_t>(c), v);
+                tmem_wait_ld();
+                if (row < P.rows) {
+                    float* yc = P.y + static_cast<int64_t>(tok0 + c) * P.ldy + row;
 #pragma unroll
-            for (int kk = 0; kk < kKStep / kMmaK; ++kk)
-                mma_f16(tmem, smem_desc_sw128(a + kk * kMmaK * 2), smem_desc_sw128(b + kk * kMmaK * 2),
-                        (kb | kk) != 0 ? 1u : 0u);
-            mma_commit(empty(s));         // the stage is free once these MMAs have read it
+                    for (int j = 0; j < 32; ++j)
+                        if (tok0 + c + j < P.M) yc[static_cast<int64_t>(j) * P.ldy] = __uint_as_float(v[j]);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(acc));
         }
-        mma_commit(done);                 // every MMA of this CTA finished (also after an abort)
     }
     __syncwarp();
-
-    // ----------------------------------------------------------- epilogue --
-    bool ok = true;
-    if (lane == 0) ok = wait_phase(done, 0u, P.timeout_ns, abort, true);
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) {
-        if (lane == 0) {
-            raise_abort(P, abort);
-            // MMAs may still run: give them time to finish before TMEM is freed
-            wait_phase(done, 0u, kDrainLimitNs, nullptr, true);
-        }
-        __syncwarp();
-    }
-    tc_fence_after_sync();
-    if (ok && !*abort) {
-        const int row = row0 + warp * 32 + lane;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        for (int c = 0; c < kTileTokens; c += 32) {
-            if (tok0 + c >= P.M) break;   // warp-uniform
-            uint32_t v[32];
-            tmem_ld32(taddr + static_cast<uint32_t>(c), v);
-            tmem_wait_ld();
-            if (row < P.rows) {
-                float* yc = P.y + static_cast<int64_t>(tok0 + c) * P.ldy + row;
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (tok0 + c + j < P.M) yc[static_cast<int64_t>(j) * P.ldy] = __uint_as_float(v[j]);
-            }
-        }
-    }
+    // ------------------------------------------------------------ teardown --
+    // no MMA may still write TMEM when it is freed
+    if (threadIdx.x == 0) wait_phase(drain, 0u, kDrainLimitNs, nullptr, true);
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -357,11 +399,12 @@ cudaError_t launch_unpack_f16(int type, const void* W, int64_t N, int64_t nb, ui
 int gemm_f16_tile_rows() { return kTileRows; }
 
 cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const uint16_t* x, int64_t M,
-                            float* y, int64_t ldy, uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
+                            float* y, int64_t ldy, uint32_t* status, int num_sms, uint64_t timeout_ns,
+                            cudaStream_t s) {
     if (rows < 1 || M < 1 || K < 1 || K > INT32_MAX || M > INT32_MAX) return cudaErrorInvalidValue;
     const int64_t gy = (rows + kTileRows - 1) / kTileRows;
     const int64_t gx = (M + kTileTokens - 1) / kTileTokens;
-    if (gy > 65535 || gx > INT32_MAX) return cudaErrorInvalidValue;
+    if (gx * gy > INT32_MAX) return cudaErrorInvalidValue;
     GemmParams P{};
     if (!encode_k_major(&P.amap, w16, rows, K, kTileRows) || !encode_k_major(&P.bmap, x, M, K, kTileTokens))
         return cudaErrorInvalidValue;
@@ -370,6 +413,8 @@ cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const 
     P.rows = static_cast<int>(rows);
     P.M = static_cast<int>(M);
     P.K = static_cast<int>(K);
+    P.tiles_tok = static_cast<int>(gx);
+    P.tiles = static_cast<int>(gx * gy);
     P.status = status;
     P.timeout_ns = timeout_ns;
     static bool attr_set = false;   // per process; the attribute is per function
@@ -378,7 +423,8 @@ cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    gemm_f16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kThreads, kSmemBytes, s>>>(P);
+    const int grid = P.tiles < num_sms ? P.tiles : (num_sms > 0 ? num_sms : 1);   // persistent: one CTA per SM
+    gemm_f16_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);
     return cudaGetLastError();
 }
 

@@ -134,4 +134,6 @@ CONFIGS = {
     4: dict(name="27B-class layer, 7 tensors, M=8", tensors=LAYER_27B, M=8),
     # the M 9 .. 16 band: one token plus 15 drafts over the same layer
     5: dict(name="27B-class layer, 7 tensors, M=16", tensors=LAYER_27B, M=16),
+    # prefill: a 4096-token prompt through one FFN gate/up tensor
+    6: dict(name="prefill: pn3t 5120->17408, M=4096", tensors=((PN3T, 5120, 17408),), M=4096, prefill=True),
 }
