@@ -306,7 +306,7 @@ pn_status pn_gemm_f16(const uint16_t* w16, int64_t N, int64_t K, const uint16_t*
     if (overlaps(y, ybytes, w16, static_cast<size_t>(N) * K * 2)) return PN_EINVAL;
     uint32_t* status = static_cast<uint32_t*>(workspace);
     const cudaError_t e = pn::launch_gemm_f16(w16, N, K, x, M, y, ldy, status, sms, g_timeout_ns.load(),
-                                              reinterpret_cast<cudaStream_t>(stream));
+                                              g_test_stall.load(), reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
 }
 
@@ -339,7 +339,8 @@ pn_status pn_prefill(int type, const void* W, int64_t N, int64_t K, const uint16
         const int64_t rows = N - r0 < chunk ? N - r0 : chunk;
         cudaError_t e = pn::launch_unpack_f16(type, static_cast<const uint8_t*>(W) + r0 * row_bytes, rows, nb, w16, s);
         if (e == cudaSuccess)
-            e = pn::launch_gemm_f16(w16, rows, K, x, M, y + r0, N, status, sms, g_timeout_ns.load(), s);
+            e = pn::launch_gemm_f16(w16, rows, K, x, M, y + r0, N, status, sms, g_timeout_ns.load(),
+                                    g_test_stall.load(), s);
         if (e != cudaSuccess) return pn::cuda_error(e);
     }
     return PN_OK;

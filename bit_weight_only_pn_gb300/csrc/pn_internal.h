@@ -96,7 +96,7 @@ cudaError_t launch_pack(int type, const float* w, int64_t N, int64_t nb, void* W
 cudaError_t launch_unpack_f16(int type, const void* W, int64_t N, int64_t nb, uint16_t* w16, cudaStream_t s);
 cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const uint16_t* x, int64_t M,
                             float* y, int64_t ldy, uint32_t* status, int num_sms, uint64_t timeout_ns,
-                            cudaStream_t s);
+                            int stall, cudaStream_t s);
 int gemm_f16_tile_rows();
 
 // CUDA-core GEMV: any nb, W and x 2-byte aligned, y 4-byte aligned.

@@ -170,6 +170,7 @@ struct GemmParams {
     int tiles;                 // tiles_tok * ceil(rows / 128)
     uint32_t* status;
     uint64_t timeout_ns;
+    int stall_first_step;      // testing aid: see pn_set_test_stall
 };
 
 // Waits for phase `parity` of an mbarrier; false after limit_ns, or at once
@@ -252,8 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
                     if (*abort) { stop = true; break; }
                     const uint32_t a = base + s * kStageBytes;
                     mbar_arrive_expect_tx(full(s), kStageBytes);
-                    tma_load_2d(a, &P.amap, kb * kKStep, row0, full(s));
-                    tma_load_2d(a + kABytes, &P.bmap, kb * kKStep, tok0, full(s));
+                    // (testing aid: with stall_first_step the first slice's
+                    // bytes are announced but never copied; its wait can only
+                    // time out)
+                    if (!(P.stall_first_step && it == 0)) {
+                        tma_load_2d(a, &P.amap, kb * kKStep, row0, full(s));
+                        tma_load_2d(a + kABytes, &P.bmap, kb * kKStep, tok0, full(s));
+                    }
                     ++it;
                 }
             }
@@ -263,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
             for (int s = 0; s < kStages; ++s) {
                 if (it <= s) continue;
                 const int last = s + kStages * ((it - 1 - s) / kStages);
+                if (P.stall_first_step && last == 0) continue;   // never copied
                 wait_phase(full(s), static_cast<uint32_t>(last / kStages) & 1u, kDrainLimitNs, nullptr, false);
             }
         }
@@ -400,7 +407,7 @@ int gemm_f16_tile_rows() { return kTileRows; }
 
 cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const uint16_t* x, int64_t M,
                             float* y, int64_t ldy, uint32_t* status, int num_sms, uint64_t timeout_ns,
-                            cudaStream_t s) {
+                            int stall, cudaStream_t s) {
     if (rows < 1 || M < 1 || K < 1 || K > INT32_MAX || M > INT32_MAX) return cudaErrorInvalidValue;
     const int64_t gy = (rows + kTileRows - 1) / kTileRows;
     const int64_t gx = (M + kTileTokens - 1) / kTileTokens;
@@ -417,6 +424,7 @@ cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const 
     P.tiles = static_cast<int>(gx * gy);
     P.status = status;
     P.timeout_ns = timeout_ns;
+    P.stall_first_step = stall;
     static bool attr_set = false;   // per process; the attribute is per function
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);

@@ -257,7 +257,7 @@ pn_status pn_prefill(int type, const void* W, int64_t N, int64_t K, const uint16
 
 /*
  * Testing aid: the time limit, in nanoseconds, of every device-side wait in
- * the tensor-core kernel (default 1e9).  A wait that runs out stops its thread
+ * the tensor-core GEMV kernels and the prefill GEMM (default 1e9).  A wait that runs out stops its thread
  * block, which records PN_ETIMEOUT in the workspace status word and returns
  * after its outstanding copies land.  Process-wide; not for concurrent use.
  */
@@ -265,10 +265,11 @@ void pn_set_wait_timeout_ns(uint64_t ns);
 
 /*
  * Testing aid for the failure path: while on (non-zero), every thread block of
- * the tensor-core kernel announces the bytes of its first step but never
- * copies them, so its consumers' wait can only end by timing out; the call
- * then reports PN_ETIMEOUT through pn_workspace_status and its outputs are
- * undefined.  Off by default.  Process-wide; not for concurrent use.
+ * the tensor-core GEMV kernels and of the prefill GEMM announces the bytes of
+ * its first step but never copies them, so its consumers' wait can only end
+ * by timing out; the call then reports PN_ETIMEOUT through
+ * pn_workspace_status and its outputs are undefined.  Off by default.
+ * Process-wide; not for concurrent use.
  */
 void pn_set_test_stall(int on);
 

@@ -133,3 +133,29 @@ def test_prefill_full_size_sampled(pn, oracle):
     toks = np.unique(np.concatenate([[0, 255, 256, M - 1], rng.integers(0, M, size=20)]))
     y_ref, abs_sum = oracle.gemm_f16(oracle.unpack_f16(PN3T, W[rows], K), x[toks])
     assert_gemm_close(y[np.ix_(toks, rows)], y_ref, abs_sum, K)
+
+
+def test_gemm_wait_timeout_reports_status(pn, oracle):
+    # Every CTA announces its first K slice's bytes but never copies them (a
+    # barrier phase nothing completes): the MMA thread's wait must give up
+    # after the time limit, the CTA must let its other copies land, free its
+    # TMEM and return, the call must report PN_ETIMEOUT, and the next call
+    # must be correct.
+    rng = np.random.default_rng(9)
+    N, K, M = 512, 1024, 300
+    w16 = (0.05 * rng.standard_normal((N, K))).astype(np.float16)
+    x = activations(rng, M, K)
+    wd, xd = torch.from_numpy(w16).to(DEV), torch.from_numpy(x).to(DEV)
+    ws = pn.Workspace(N, DEV)
+    try:
+        pn.set_wait_timeout_ns(2_000_000)
+        pn.set_test_stall(True)
+        pn.gemm_f16(wd, xd, workspace=ws)
+        assert ws.status() == 5
+    finally:
+        pn.set_test_stall(False)
+        pn.set_wait_timeout_ns(1_000_000_000)
+    y = pn.gemm_f16(wd, xd, workspace=ws).cpu().numpy()
+    assert ws.status() == 0
+    y_ref, abs_sum = oracle.gemm_f16(w16, x)
+    assert_gemm_close(y, y_ref, abs_sum, K)
