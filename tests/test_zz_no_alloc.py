@@ -5,7 +5,7 @@ stream owned by another runtime, plugins whose framework owns every
 allocation, serving loops that must not touch the allocator after loading), so
 they cannot hand pn_gemv its workspace.  pn_gemv_noalloc takes its scratch from
 a fixed array in the library instead.  This test calls it through the C ABI,
-three times in a row with different shapes (the array keeps the previous
+four times in a row with different shapes (the array keeps the previous
 call's contents), and checks each result against pn_gemv's on the same inputs within
 the GEMV tolerance used by every other GPU test.  The file name makes pytest
 collect it last; it also passes when run on its own in a fresh process.
@@ -46,9 +46,10 @@ def test_noalloc_matches_pn_gemv_twice(pn, oracle):
     # different shapes in a row; all split tiles across thread blocks, so each
     # call runs on hand-off words, counters and slots an earlier one used (the
     # first two go through the multi-token kernel, the third through the
-    # one-token kernel)
+    # one-token kernel, the fourth through the multi-token kernel's 16-token
+    # form)
     for pn_type, N, K, M, seed in ((PN3T, 2000, 40 * 80, 3, 0xA11), (PN4T, 777, 24 * 64, 8, 0xA12),
-                                   (PN3T, 3001, 64 * 80, 1, 0xA13)):
+                                   (PN3T, 3001, 64 * 80, 1, 0xA13), (PN4T, 1500, 32 * 64, 16, 0xA14)):
         w = synth.weights(seed, N, K)
         x = synth.activations(seed + 8, M, K)
         W = oracle.pack(pn_type, w)
