@@ -98,28 +98,46 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of every CUDA source of the library: a recorded ncu traffic figure
-    is only used while the kernels it was taken on are unchanged."""
+# The sources each workload's timed kernel is built from (its own file plus
+# the shared device and host headers).
+KERNEL_SOURCES = {
+    "stream": ("pn_gemv_stream.cu", "pn_device.cuh", "pn_internal.h"),
+    "tc": ("pn_gemv_tc.cu", "pn_device.cuh", "pn_internal.h"),
+    "prefill": ("pn_prefill.cu", "pn_device.cuh", "pn_internal.h"),
+}
+
+
+def kernel_of(cfg: int) -> str:
+    """Which kernel a workload times: the one-token kernel (M <= 2), the
+    batch kernel (M = 3 .. 16) or the prefill GEMM."""
+    from bit_weight_only_pn_gb300 import synth
+    c = synth.CONFIGS[cfg]
+    if c.get("prefill"):
+        return "prefill"
+    return "stream" if c["M"] <= 2 else "tc"
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is built from: a recorded ncu traffic
+    figure is only used while they are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_weight_only_pn_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(cfg: int):
-    """Per-launch DRAM bytes (read + write) of the workload's GEMV kernel from
-    the committed ncu summary, if it was taken on the current kernel sources
-    (else None)."""
+    """Per-launch DRAM bytes (read + write) of the workload's timed kernel from
+    the committed ncu summary, if it was taken on that kernel's current
+    sources (else None)."""
     path = os.path.join(ROOT, "profiles", "pn_gemv_traffic.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel_of(cfg))
     for m in re.finditer(r"^traffic config=(\d+) kernel=(\S+) bytes_per_launch=(\d+) source=([0-9a-f]+)",
                          text, re.M):
         if int(m.group(1)) == cfg and m.group(4) == want:
@@ -416,7 +434,7 @@ def run_prefill(args, world, rank, local):
         peak, peak_src = 1900.0, "fallback 1.9 PFLOP/s bf16 burst"
     achieved = flops / (ms_gemm / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                "frac": achieved / peak, "traffic": recorded_traffic(args.config), "peak_source": peak_src,
                 "kernel": "gemm_f16_kernel", "kernel_ms": ms_gemm}
 
     cpu = None
