@@ -117,14 +117,41 @@ def kernel_of(cfg: int) -> str:
     return "stream" if c["M"] <= 2 else "tc"
 
 
+def code_only(text: str) -> str:
+    """C/C++ source with comments removed and whitespace collapsed (string
+    and character literals kept), so that editing a comment does not count
+    as changing a kernel."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """Hash of the sources a kernel is built from: a recorded ncu traffic
-    figure is only used while they are unchanged."""
+    """Hash of the code (comments and layout aside) of the sources a kernel
+    is built from: a recorded ncu traffic figure is only used while that code
+    is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_weight_only_pn_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
