@@ -24,7 +24,8 @@
 //    the shared tiles are settled early.
 //  * One producer warp issues, per step, one tiled 2-D TMA copy per tile (a
 //    tensor map over the PN rows, 16-row x 272-byte box) and one bulk copy per
-//    activation row into a 4-stage shared-memory ring completing on mbarriers.
+//    activation row into a shared-memory ring (4 stages for M <= 8, 3 above)
+//    completing on mbarriers.
 //    Sixteen consumer warps, two per tile, each decode four of a chunk's eight
 //    blocks.  An epilogue warp adds each tile's two halves (fixed order) and
 //    stores it, or, for a shared tile, deposits its part and lets the last of

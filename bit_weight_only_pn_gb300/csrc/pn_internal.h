@@ -126,7 +126,7 @@ cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* 
 int stream_max_ctas(int num_sms);
 size_t stream_tagged_bytes(int num_sms);
 
-// Tensor-core GEMV for 3 <= M <= 8 (same eligibility): thread blocks share
+// Tensor-core GEMV for 3 <= M <= 16 (same eligibility): thread blocks share
 // each staged activation chunk among eight tiles.
 cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* status, float* partials,
                            uint32_t* counters, int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s);
