@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--m", type=int, default=0,
+                    help="GEMV workloads: override the token count M (1 .. 16); 0 keeps the workload's")
     ap.add_argument("--hadamard", type=int, default=0,
                     help="rotate every tensor's activations with pn_hadamard (this block size) "
                          "before its GEMV, inside each step (0 = off)")
@@ -70,10 +72,30 @@ def parse_args():
 
 # ----------------------------------------------------------------- helpers ---
 
-def workload(cfg: int):
+def workload(cfg: int, m_override: int = 0):
     from bit_weight_only_pn_gb300 import synth
     c = synth.CONFIGS[cfg]
+    if m_override and not c.get("prefill"):
+        if not 1 <= m_override <= 16:
+            raise SystemExit("--m must be in 1 .. 16")
+        return f"{c['name']} (run at M={m_override})", list(c["tensors"]), m_override
     return c["name"], list(c["tensors"]), c["M"]
+
+
+def cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo (model name, else the Arm part number)."""
+    try:
+        text = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    m = re.search(r"^model name\s*:\s*(.+)$", text, re.M)
+    if m:
+        return m.group(1).strip()
+    impl = re.search(r"^CPU implementer\s*:\s*(\S+)", text, re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", text, re.M)
+    if impl and part:
+        return f"Arm implementer {impl.group(1)} part {part.group(1)}"
+    return "unknown"
 
 
 def per_block(t: int) -> int:
@@ -320,7 +342,7 @@ def run_reference(args, world, rank):
         return
     import oracle
     from bit_weight_only_pn_gb300 import synth
-    name, tensors, M = workload(args.config)
+    name, tensors, M = workload(args.config, args.m)
     o = oracle.Oracle()
     threads = os.cpu_count() or 1
     t0, K0, N0 = tensors[0]
@@ -542,7 +564,8 @@ def run_ours(args, world, rank, local):
     dist_barrier(world)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    name, tensors, M = workload(args.config)
+    name, tensors, M = workload(args.config, args.m)
+    default_m = workload(args.config)[2] == M
     algo = {"auto": pn.ALGO_AUTO, "tc": pn.ALGO_TENSOR_CORE, "cuda_core": pn.ALGO_CUDA_CORE}[args.algo]
     step_bytes = algorithmic_bytes(tensors, M)
     wbytes = sum(N * (K // per_block(t)) * 34 for t, K, N in tensors)
@@ -679,17 +702,50 @@ def run_ours(args, world, rank, local):
                "path": "pinned x -> device, pn_gemv via the Python binding, y -> pinned host, "
                        "stream synchronised each step; weights resident"}
 
+    # read-only ceiling on the same box and buffers: one pn_read_ranges
+    # launch per step reads the step's weight copies once (16-byte loads, no
+    # decode), in CUDA graphs like the GEMV steps
+    sink = torch.zeros(len(tensors), dtype=torch.int32, device=dev)
+
+    def read_step(i):
+        pn.read_ranges([W for (_, W, _, _, _) in rot[i % copies]], sink, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(3 * copies):
+            read_step(i)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(nodes):
+                read_step(i)
+        gr.replay()
+        torch.cuda.synchronize(dev)
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r_reps = max(1, reps)
+        r0.record(stream)
+        for _ in range(r_reps):
+            gr.replay()
+        r1.record(stream)
+        torch.cuda.synchronize(dev)
+    r_us = r0.elapsed_time(r1) * 1e3 / (r_reps * nodes)
+    read_ceiling = {"us_per_step": r_us, "gbs": wbytes / (r_us / 1e6) / 1e9,
+                    "time_frac": r_us / (ms_per_step * 1e3),
+                    "how": "pn_read_ranges over the same rotating PN weight copies (one launch per "
+                           "step, 16-byte loads, no decode), CUDA graphs; time_frac = read time / GEMV time"}
+
     peak, peak_kind = measured_peak()
     per_gpu = step_bytes / (ms_per_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s",
-                "frac": per_gpu / peak, "traffic": recorded_traffic(args.config),
+                "frac": per_gpu / peak, "traffic": recorded_traffic(args.config) if default_m else None,
                 "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc, used, _ = oracle_sample_rate(tensors, M, args.cpu_seconds, os.cpu_count() or 1)
-        cpu = {"value": rate, "unit": "GB/s", "cores": used, "kind": "oracle", "sample": desc}
+        rate1, desc1, _, _ = oracle_sample_rate(tensors, M, args.cpu_seconds / 2, 1)
+        cpu = {"value": rate, "unit": "GB/s", "cores": used, "kind": "oracle", "sample": desc,
+               "value_one_core": rate1, "sample_one_core": desc1, "cpu_model": cpu_model()}
 
     if rank != 0:
         return
@@ -711,6 +767,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": args.steps * ((1 if len(tensors) == 1 or algo != pn.ALGO_CUDA_CORE else len(tensors))
                                       + (len(tensors) if args.hadamard else 0)),
         "roofline": roofline,
+        "read_ceiling": read_ceiling,
         "clocks": clock_info,
         "e2e": e2e,
         "cpu_baseline": cpu,

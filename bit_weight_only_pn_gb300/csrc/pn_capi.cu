@@ -346,6 +346,21 @@ pn_status pn_prefill(int type, const void* W, int64_t N, int64_t K, const uint16
     return PN_OK;
 }
 
+pn_status pn_read_ranges(const void* const* ptrs, const size_t* bytes, int count, uint32_t* sink,
+                         pn_stream stream) {
+    if (!ptrs || !bytes || !sink || count < 1 || count > PN_MAX_LAYER) return PN_EINVAL;
+    for (int e = 0; e < count; ++e) {
+        if (!ptrs[e] && bytes[e] >= 16) return PN_EINVAL;
+        if (!aligned(ptrs[e], 16)) return PN_EALIGN;
+    }
+    if (!aligned(sink, 4)) return PN_EALIGN;
+    int sms = 0, major = 0;
+    pn_status st = device_info(&sms, &major);
+    if (st != PN_OK) return st;
+    const cudaError_t e = pn::launch_read_ranges(ptrs, bytes, count, sink, sms, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
+}
+
 const char* pn_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 void pn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }

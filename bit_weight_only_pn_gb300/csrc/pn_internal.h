@@ -99,6 +99,10 @@ cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const 
                             int stall, cudaStream_t s);
 int gemm_f16_tile_rows();
 
+// Read-bandwidth probe: every 16-byte word of `count` ranges read once, XORs into sink[e].
+cudaError_t launch_read_ranges(const void* const* ptrs, const size_t* bytes, int count, uint32_t* sink,
+                               int num_sms, cudaStream_t s);
+
 // CUDA-core GEMV: any nb, W and x 2-byte aligned, y 4-byte aligned.
 cudaError_t launch_gemv_simt(const GemvTensor& t, int M, cudaStream_t s);
 

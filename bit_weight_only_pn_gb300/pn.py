@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
             L.pn_gemm_f16.argtypes = [vp, i64, i64, vp, i64, vp, i64, vp, sz, vp]
             L.pn_prefill.restype = i32
             L.pn_prefill.argtypes = [i32, vp, i64, i64, vp, i64, vp, vp, sz, vp, sz, vp]
+            L.pn_read_ranges.restype = i32
+            L.pn_read_ranges.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(sz), i32, vp, vp]
             L.pn_hadamard.restype = i32
             L.pn_hadamard.argtypes = [vp, i32, i64, i32, vp, vp]
             L.pn_set_wait_timeout_ns.restype = None
@@ -273,6 +275,19 @@ def prefill(pn_type: int, W: torch.Tensor, K: int, x: torch.Tensor, y: torch.Ten
                             scratch.numel() * 2, workspace.ptr, workspace.nbytes, _stream(stream)),
            "pn_prefill")
     return y
+
+
+def read_ranges(tensors, sink: torch.Tensor, stream=None) -> torch.Tensor:
+    """Diagnostic read-bandwidth probe (see pn_read_ranges): reads every
+    tensor's bytes once and XORs its 32-bit words into sink[i] (int32 device
+    tensor with one element per tensor)."""
+    tensors = list(tensors)
+    n = len(tensors)
+    ptrs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in tensors])
+    sizes = (ctypes.c_size_t * n)(*[t.numel() * t.element_size() for t in tensors])
+    _require(sink, torch.int32, "sink")
+    _check(lib().pn_read_ranges(ptrs, sizes, n, sink.data_ptr(), _stream(stream)), "pn_read_ranges")
+    return sink
 
 
 def set_wait_timeout_ns(ns: int) -> None:

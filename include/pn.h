@@ -256,6 +256,17 @@ pn_status pn_prefill(int type, const void* W, int64_t N, int64_t K, const uint16
                      pn_stream stream);
 
 /*
+ * pn_read_ranges (diagnostic): the plain read-bandwidth ceiling a GEMV is
+ * measured against.  Reads the first floor(bytes[i] / 16) * 16 bytes of each
+ * of `count` (1 .. PN_MAX_LAYER) device ranges ptrs[i] once, with 16-byte
+ * loads, and XORs the 32-bit words read into sink[i] (device, `count` words;
+ * zero them first if the value matters).  ptrs and bytes are host arrays
+ * read during the call; every ptrs[i] 16-byte aligned, sink 4-byte aligned.
+ */
+pn_status pn_read_ranges(const void* const* ptrs, const size_t* bytes, int count, uint32_t* sink,
+                         pn_stream stream);
+
+/*
  * Testing aid: the time limit, in nanoseconds, of every device-side wait in
  * the tensor-core GEMV kernels and the prefill GEMM (default 1e9).  A wait that runs out stops its thread
  * block, which records PN_ETIMEOUT in the workspace status word and returns

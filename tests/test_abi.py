@@ -125,3 +125,16 @@ def test_prefill_checks(lib):
     assert g(FAKE, 0, 128, FAKE * 2, 4, FAKE * 4, 16, ws, 1 << 20, None) == 0
     assert p(124, FAKE, 16, 100, FAKE * 2, 4, FAKE * 4, FAKE * 16, 1 << 20, ws, 1 << 20, None) == PN_EINVAL
     assert p(125, FAKE, 16, 128, FAKE * 2, 0, FAKE * 4, FAKE * 16, 1 << 20, ws, 1 << 20, None) == PN_EINVAL
+
+
+def test_read_ranges_checks(lib):
+    r = lib.pn_read_ranges
+    ptrs = (ctypes.c_void_p * 2)(FAKE, FAKE * 2)
+    sizes = (ctypes.c_size_t * 2)(1024, 1024)
+    assert r(ptrs, sizes, 0, FAKE * 4, None) == PN_EINVAL           # no ranges
+    assert r(ptrs, sizes, 9, FAKE * 4, None) == PN_EINVAL           # more than PN_MAX_LAYER
+    assert r(None, sizes, 2, FAKE * 4, None) == PN_EINVAL
+    assert r(ptrs, sizes, 2, None, None) == PN_EINVAL
+    bad = (ctypes.c_void_p * 2)(FAKE, FAKE * 2 + 8)
+    assert r(bad, sizes, 2, FAKE * 4, None) == PN_EALIGN            # range not 16-byte aligned
+    assert r(ptrs, sizes, 2, FAKE * 4 + 2, None) == PN_EALIGN       # sink not 4-byte aligned
