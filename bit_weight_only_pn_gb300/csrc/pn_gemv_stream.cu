@@ -752,13 +752,9 @@ bool encode_rows(CUtensorMap* map, const GemvTensor& t) {
 
 template <int BPM>
 cudaError_t launch_bpm(const SParams& P, cudaStream_t s) {
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BPM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = set_smem_limit_once(gemv_stream_kernel<BPM>, kSmemBytes, smem_set); e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(P.grid);
     cfg.blockDim = dim3(kThreads);

@@ -893,15 +893,12 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* stat
     P.timeout_ns = timeout_ns;
     P.stall_first_step = stall;
 
-    static bool attr_set[2] = {false, false};   // per process; the attribute is per function
+    static std::atomic<uint64_t> smem_set[2] = {{0}, {0}};
     const int smem_bytes = nt == 1 ? Smem<1>::kBytes : Smem<2>::kBytes;
-    if (!attr_set[nt - 1]) {
-        cudaError_t e = nt == 1
-            ? cudaFuncSetAttribute(gemv_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
-            : cudaFuncSetAttribute(gemv_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        if (e != cudaSuccess) return e;
-        attr_set[nt - 1] = true;
-    }
+    if (cudaError_t e = nt == 1 ? set_smem_limit_once(gemv_tc_kernel<1>, smem_bytes, smem_set[0])
+                                : set_smem_limit_once(gemv_tc_kernel<2>, smem_bytes, smem_set[1]);
+        e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(P.grid);
     cfg.blockDim = dim3(kThreads);

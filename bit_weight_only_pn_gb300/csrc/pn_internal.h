@@ -1,6 +1,7 @@
 // pn_internal.h -- host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -71,6 +72,22 @@ struct CostSplit {
         return grid;
     }
 };
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (the attribute belongs to each device's copy of
+// the kernel); `done` holds one bit per device already set.
+template <typename Kernel>
+cudaError_t set_smem_limit_once(Kernel* kernel, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // One tensor of a GEMV launch, as the host hands it to a kernel.
 struct GemvTensor {

@@ -425,12 +425,8 @@ cudaError_t launch_gemm_f16(const uint16_t* w16, int64_t rows, int64_t K, const 
     P.status = status;
     P.timeout_ns = timeout_ns;
     P.stall_first_step = stall;
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = set_smem_limit_once(gemm_f16_kernel, kSmemBytes, smem_set); e != cudaSuccess) return e;
     const int grid = P.tiles < num_sms ? P.tiles : (num_sms > 0 ? num_sms : 1);   // persistent: one CTA per SM
     gemm_f16_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);
     return cudaGetLastError();
