@@ -233,7 +233,7 @@ def big_inputs(oracle):
     return get
 
 
-@pytest.mark.parametrize("M", [1, 8, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 16])
 @pytest.mark.parametrize("cfg", [0, 1, 2])
 def test_gemv_full_size_sampled(pn, dev, oracle, big_inputs, cfg, M):
     from bit_weight_only_pn_gb300 import synth
@@ -248,10 +248,10 @@ def test_gemv_full_size_sampled(pn, dev, oracle, big_inputs, cfg, M):
     assert_gemv_close(y[:, rows], y_ref, abs_sum)
 
 
-@pytest.mark.parametrize("M", [1, 8, 16])
+@pytest.mark.parametrize("M", [1, 2, 8, 16])
 def test_layer_full_size_sampled(pn, dev, oracle, big_inputs, M):
     from bit_weight_only_pn_gb300 import synth
-    cfg = {1: 3, 8: 4, 16: 5}[M]
+    cfg = {1: 3, 2: 3, 8: 4, 16: 5}[M]
     entries, host = [], []
     total_rows = 0
     for e, (pn_type, K, N) in enumerate(synth.LAYER_27B):
