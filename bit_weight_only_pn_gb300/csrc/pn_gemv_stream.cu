@@ -141,9 +141,13 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     }
 }
 
-// Lane 0 polls; __syncwarp orders the other lanes' reads of the stage after
-// lane 0's observation of the completed phase.
+// Fast path: every lane probes once and the warp votes; if the phase has
+// completed, each lane has observed it itself and the warp goes on at once.
+// Otherwise lane 0 polls and __syncwarp orders the other lanes' reads of the
+// stage after lane 0's observation of the completed phase.  Every lane of the
+// warp must call it.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, int lane) {
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
     bool ok = true;
     if (lane == 0) ok = wait_bounded(bar, parity, limit_ns);
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
