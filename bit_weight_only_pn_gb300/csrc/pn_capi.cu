@@ -367,4 +367,21 @@ void pn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
 
 void pn_set_test_stall(int on) { g_test_stall.store(on ? 1 : 0); }
 
+pn_status pn_tc_split(const int* types, const int64_t* N, const int64_t* K, int count, int M, int num_sms,
+                      uint32_t* starts, int* grid) {
+    if (!types || !N || !K || !starts || !grid) return PN_EINVAL;
+    if (count < 1 || count > PN_MAX_LAYER || M < 3 || M > PN_MAX_M || num_sms < 1) return PN_EINVAL;
+    pn::GemvTensor ts[pn::kMaxLayer] = {};
+    for (int e = 0; e < count; ++e) {
+        const int bpb = per_block(types[e]);
+        if (bpb == 0 || K[e] <= 0 || K[e] % (8 * bpb) != 0 || N[e] < 1) return PN_EINVAL;
+        const int64_t nb = K[e] / bpb;
+        if (N[e] > INT32_MAX / 2 || nb > INT32_MAX / 8) return PN_EINVAL;
+        ts[e].type = types[e];
+        ts[e].N = static_cast<int>(N[e]);
+        ts[e].nb = static_cast<int>(nb);
+    }
+    return pn::tc_split(ts, count, M, num_sms, grid, starts) ? PN_OK : PN_EINVAL;
+}
+
 }  // extern "C"

@@ -15,9 +15,12 @@
 //    row, 16-byte aligned whenever the row is).  Units are numbered tile-major
 //    over every tensor of the call and the persistent grid (at most one CTA per
 //    SM, each range at least one tile long) splits them into contiguous
-//    ranges of equal decode cost (a pn3t unit weighs more than a pn4t one), so
-//    every SM finishes at about the same time and only a CTA's first and last
-//    tile can be shared, each with one neighbour.
+//    ranges of equal modelled time (each unit's decode, a pn3t unit weighing
+//    more than a pn4t one, plus a cost per batch step, since a step with few
+//    tiles at work takes nearly as long as a full one), so every SM finishes
+//    at about the same time and only a CTA's first and last tile can be
+//    shared, each with one neighbour.  The split is searched on the host once
+//    per call shape and cached.
 //  * A CTA walks its tiles in batches of up to 8 consecutive tiles of one
 //    tensor, chunk by chunk (one step = one chunk of the batch's tiles, so the
 //    activation chunk is staged once for 8 tiles), last batch first so that
@@ -44,6 +47,8 @@
 //    still cross HBM once; the stage holds 16 activation rows and the ring
 //    has three stages instead of four to stay within shared memory.
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -76,12 +81,19 @@ constexpr int kOutBuffers = 2;
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                  // PN_ETIMEOUT
 constexpr int kSlotFloats = kTileRows * kMaxM;          // 256: one tile's partial sums
-// Relative cost of one unit, pn3t / pn4t, for the split of the units over
-// the thread blocks (5 / 4 MMAs per block and column tile and their code
-// pairs, plus the per-block work both share).  Measured on a mixed pn3t / pn4t
-// layer at 8 and 16 tokens, 16 / 15 was about 4 % faster than an even split
-// of the units; larger ratios (8 / 7 and up) were slower again.
-constexpr uint32_t kCostPn3t = 16, kCostPn4t = 15;
+// Weights of the work split (RangeModel): the cost of one batch step and of
+// one pn3t / pn4t unit, for one and two column tiles.  A step costs several
+// units because a batch step takes most of a full step's time even when few
+// of its tiles have work.  The values were chosen by timing the kernel over a
+// grid of weights (step 0 .. 180, pn3t 16 .. 28 against pn4t 15) on two
+// mixed pn3t / pn4t layers (27B-class, hidden 5120; and hidden 2560) at 3, 8,
+// 12 and 16 tokens: against an even split of the units at 16 / 15 they made
+// the 27B-class layer 11 - 15 % faster with one column tile and 6 - 8 % with
+// two, and the small layer 1 - 2 % faster.
+struct SplitWeights {
+    uint32_t step, pn3t, pn4t;
+};
+constexpr SplitWeights kSplitWeights[2] = {{126, 20, 15}, {90, 22, 15}};
 constexpr int kMaxGrid = 256;                           // thread blocks per launch, at most
 
 // Shared-memory layout of the kernel with NT 8-column tiles (M <= 8 NT).
@@ -856,6 +868,170 @@ bool encode_x(CUtensorMap* map, const GemvTensor& t, int M) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ------------------------------------------------------------ work split --
+
+// Host model of the time one CTA spends on the units [u0, u1): it walks them
+// in the kernel's batches (Walker) and charges every batch step step_cost
+// and every unit its decode cost.  A step takes about as long with one tile
+// at work as with several (the other warp pairs idle), so ranges whose tiles
+// fill few batches finish early and ranges that add a short batch finish
+// late; the split below balances this modelled time, not the unit count.
+struct RangeModel {
+    uint32_t base[kMaxLayer + 1];   // first unit of each tensor; base[count] = all
+    uint32_t unit_cost[kMaxLayer];
+    uint32_t step_cost;
+    int tiles[kMaxLayer], chunks[kMaxLayer];
+    int count;
+    int lane_rows;                  // staged activation rows / M (chunk lanes allowed)
+
+    void locate(uint32_t u, int& e, int& tile, int& c) const {
+        e = 0;
+        while (e + 1 < count && u >= base[e + 1]) ++e;
+        const uint32_t rel = u - base[e];
+        tile = static_cast<int>(rel / static_cast<uint32_t>(chunks[e]));
+        c = static_cast<int>(rel - static_cast<uint32_t>(tile) * chunks[e]);
+    }
+
+    uint64_t cost(uint32_t u0, uint32_t u1) const {
+        if (u1 <= u0) return 0;
+        int e0, t0, c0, e1, t1, c1;
+        locate(u0, e0, t0, c0);
+        locate(u1 - 1, e1, t1, c1);
+        uint64_t steps = 0;
+        // windows of 8 tiles from the first tile, then from tile 0 of each
+        // later tensor, as the kernel walks them (order does not matter here)
+        for (int e = e0, tb = t0;;) {
+            int nt = tiles[e] - tb < kBatchTiles ? tiles[e] - tb : kBatchTiles;
+            const bool last = e == e1 && t1 - tb < kBatchTiles;
+            if (last) nt = t1 - tb + 1;
+            const int cs0 = (e == e0 && tb == t0) ? c0 : 0;
+            const int ce = last ? c1 + 1 : chunks[e];
+            int cap = kBatchTiles / nt;
+            cap = cap < lane_rows ? cap : lane_rows;
+            cap = cap < chunks[e] ? cap : chunks[e];
+            const int lanes = cap >= 8 ? 8 : cap >= 4 ? 4 : cap >= 2 ? 2 : 1;
+            const int span = nt == 1 ? ce - cs0 : chunks[e];
+            steps += static_cast<uint64_t>((span + lanes - 1) / lanes);
+            if (last) break;
+            tb += kBatchTiles;
+            if (tb >= tiles[e]) { ++e; tb = 0; }
+        }
+        uint64_t c = steps * step_cost;
+        for (int e = e0; e <= e1; ++e) {
+            const uint32_t a = u0 > base[e] ? u0 : base[e];
+            const uint32_t b = u1 < base[e + 1] ? u1 : base[e + 1];
+            c += static_cast<uint64_t>(b - a) * unit_cost[e];
+        }
+        return c;
+    }
+
+    // The largest v in [u + min_units, units] with cost(u, v) <= limit that
+    // leaves no remainder shorter than min_units; 0 when there is none.
+    uint32_t extent(uint32_t u, uint64_t limit, uint32_t min_units) const {
+        const uint32_t units = base[count];
+        uint32_t ok = u + min_units;
+        if (ok > units || cost(u, ok) > limit) return 0;
+        uint32_t bad = units + 1;                        // first v known to fail
+        for (uint32_t step = min_units; ok < units;) {   // gallop, then bisect
+            const uint32_t v = units - ok > step ? ok + step : units;
+            if (cost(u, v) <= limit) { ok = v; step *= 2; }
+            else { bad = v; break; }
+        }
+        while (bad - ok > 1) {
+            const uint32_t v = ok + (bad - ok) / 2;
+            if (cost(u, v) <= limit) ok = v;
+            else bad = v;
+        }
+        if (ok < units && units - ok < min_units) {      // the rest must be a range too
+            ok = units - min_units;
+            if (ok < u + min_units) return 0;
+        }
+        return ok;
+    }
+
+    // Packs the units greedily into ranges of modelled cost <= limit; the
+    // number of ranges, or 0 when more than max_ranges would be needed.
+    int pack(uint64_t limit, int max_ranges, uint32_t min_units, uint32_t* starts) const {
+        const uint32_t units = base[count];
+        uint32_t u = 0;
+        int n = 0;
+        starts[0] = 0;
+        while (u < units) {
+            if (n == max_ranges) return 0;
+            const uint32_t v = extent(u, limit, min_units);
+            if (v == 0) return 0;
+            starts[++n] = v;
+            u = v;
+        }
+        return n;
+    }
+};
+
+// A split of the units over the thread blocks, kept per call shape: the
+// search below costs some hundred microseconds of host time, a lookup none.
+struct SplitKey {
+    int count, M, max_grid;
+    int type[kMaxLayer], nb[kMaxLayer], N[kMaxLayer];
+};
+struct SplitEntry {
+    SplitKey key;
+    int grid;
+    uint32_t starts[kMaxGrid + 1];
+};
+constexpr int kSplitCacheEntries = 16;
+
+// Fills grid and starts: the cost-weighted split (CostSplit) unless the
+// greedy packing of RangeModel, searched over its cost limit, gives a lower
+// largest range cost.  Both keep every range at least min_units long, so a
+// tile has at most two owners.
+void balanced_split(const RangeModel& m, int max_grid, uint32_t min_units, int& grid, uint32_t* starts) {
+    CostSplit even{};
+    for (int e = 0; e < m.count; ++e) even.add(m.base[e + 1] - m.base[e], m.unit_cost[e]);
+    grid = even.fit_grid(max_grid, min_units);
+    uint64_t hi = 0;
+    for (int c = 0; c <= grid; ++c) starts[c] = even.start(c);
+    for (int c = 0; c < grid; ++c) {
+        const uint64_t v = m.cost(starts[c], starts[c + 1]);
+        hi = v > hi ? v : hi;
+    }
+    uint64_t lo = (even.cbase[even.count] + static_cast<uint64_t>(max_grid) - 1) / static_cast<uint64_t>(max_grid);
+    static thread_local uint32_t trial[kMaxGrid + 1];
+    while (lo < hi) {                                  // smallest limit that packs
+        const uint64_t mid = lo + (hi - lo) / 2;
+        const int n = m.pack(mid, max_grid, min_units, trial);
+        if (n > 0) {
+            hi = mid;
+            grid = n;
+            for (int c = 0; c <= n; ++c) starts[c] = trial[c];
+        } else {
+            lo = mid + 1;
+        }
+    }
+}
+
+void cached_split(const SplitKey& key, const RangeModel& m, uint32_t min_units, int& grid, uint32_t* starts) {
+    static std::mutex mu;
+    static SplitEntry cache[kSplitCacheEntries];
+    static int filled = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < filled; ++i)
+            if (std::memcmp(&cache[i].key, &key, sizeof key) == 0) {
+                grid = cache[i].grid;
+                std::memcpy(starts, cache[i].starts, sizeof(uint32_t) * (grid + 1));
+                return;
+            }
+    }
+    balanced_split(m, key.max_grid, min_units, grid, starts);
+    std::lock_guard<std::mutex> lock(mu);
+    SplitEntry& slot = cache[next];
+    next = (next + 1) % kSplitCacheEntries;
+    filled = filled < kSplitCacheEntries ? filled + 1 : filled;
+    slot.key = key;
+    slot.grid = grid;
+    std::memcpy(slot.starts, starts, sizeof(uint32_t) * (grid + 1));
+}
+
 }  // namespace
 
 int tc_max_ctas(int num_sms) { return num_sms < kMaxGrid ? num_sms : kMaxGrid; }
@@ -864,11 +1040,43 @@ size_t tc_partial_bytes(int num_sms) {
     return static_cast<size_t>(tc_max_ctas(num_sms) + 1) * 2 * kSlotFloats * sizeof(float);
 }
 
+bool tc_split(const GemvTensor* t, int count, int M, int num_sms, int* grid, uint32_t* starts) {
+    const int nt = M > 8 ? 2 : 1;                  // 8-column tiles
+    const SplitWeights& wt = kSplitWeights[nt - 1];
+    RangeModel model{};
+    SplitKey key{};                                // zero-filled: compared bytewise
+    model.count = key.count = count;
+    model.lane_rows = 8 * nt / M;                  // staged activation rows / M
+    model.step_cost = wt.step;
+    key.M = M;
+    key.max_grid = tc_max_ctas(num_sms);
+    uint64_t units = 0;
+    int max_chunks = 1;
+    for (int e = 0; e < count; ++e) {
+        const int chunks = t[e].nb / kChunkBlocks;
+        const int tiles = (t[e].N + kTileRows - 1) / kTileRows;
+        if (chunks < 1 || tiles < 1) return false;
+        model.base[e] = static_cast<uint32_t>(units);
+        model.unit_cost[e] = t[e].type == kPn3t ? wt.pn3t : wt.pn4t;
+        model.tiles[e] = tiles;
+        model.chunks[e] = chunks;
+        key.type[e] = t[e].type;
+        key.nb[e] = t[e].nb;
+        key.N[e] = t[e].N;
+        units += static_cast<uint64_t>(chunks) * tiles;
+        max_chunks = chunks > max_chunks ? chunks : max_chunks;
+    }
+    if (units >= (1ull << 32)) return false;      // 32-bit unit numbers
+    model.base[count] = static_cast<uint32_t>(units);
+    // every range spans at least one whole tile, so a tile has at most two owners
+    cached_split(key, model, static_cast<uint32_t>(max_chunks), *grid, starts);
+    return true;
+}
+
 cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* status, float* partials,
                            uint32_t* counters, int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s) {
     TcParams P{};
     uint64_t units = 0;
-    int max_chunks = 1;
     for (int e = 0; e < count; ++e) {
         TcTensor& T = P.t[e];
         T.W = t[e].W; T.x = t[e].x; T.y = t[e].y;
@@ -880,19 +1088,12 @@ cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* stat
             if (!encode_rows(&P.wmap[k][e], t[e], kTileRows << k)) return cudaErrorInvalidValue;
         if (!encode_x(&P.xmap[e], t[e], M)) return cudaErrorInvalidValue;
         units += static_cast<uint64_t>(T.chunks) * T.tiles;
-        max_chunks = T.chunks > max_chunks ? T.chunks : max_chunks;
     }
     P.count = count;
     P.M = M;
     const int nt = M > 8 ? 2 : 1;                  // 8-column tiles
     P.x_rows = 8 * nt;
-    if (units >= (1ull << 32)) return cudaErrorInvalidValue;   // 32-bit unit numbers
-    CostSplit split{};
-    for (int e = 0; e < count; ++e)
-        split.add(static_cast<uint32_t>(P.t[e].chunks) * P.t[e].tiles, P.t[e].type == kPn3t ? kCostPn3t : kCostPn4t);
-    // every range spans at least one whole tile, so a tile has at most two owners
-    P.grid = split.fit_grid(tc_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
-    for (int c = 0; c <= P.grid; ++c) P.starts[c] = split.start(c);
+    if (!tc_split(t, count, M, num_sms, &P.grid, P.starts)) return cudaErrorInvalidValue;
     P.status = status;
     P.counters = counters;
     P.partials = partials;

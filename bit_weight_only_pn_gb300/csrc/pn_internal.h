@@ -152,6 +152,10 @@ size_t stream_tagged_bytes(int num_sms);
 cudaError_t launch_gemv_tc(const GemvTensor* t, int count, int M, uint32_t* status, float* partials,
                            uint32_t* counters, int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s);
 int tc_max_ctas(int num_sms);
+// The tensor-core GEMV's split of the units of tensors t[0 .. count) over its
+// thread blocks (host only): *grid blocks, block c taking units
+// [starts[c], starts[c + 1]); false when the tensors are empty or too large.
+bool tc_split(const GemvTensor* t, int count, int M, int num_sms, int* grid, uint32_t* starts);
 size_t tc_partial_bytes(int num_sms);
 
 }  // namespace pn

@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
             L.pn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
             L.pn_set_test_stall.restype = None
             L.pn_set_test_stall.argtypes = [ctypes.c_int]
+            L.pn_tc_split.restype = i32
+            L.pn_tc_split.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64), i32, i32,
+                                      i32, ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(i32)]
             _lib = L
         return _lib
 
@@ -296,3 +299,19 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def set_test_stall(on: bool) -> None:
     lib().pn_set_test_stall(1 if on else 0)
+
+
+def tc_split(shapes, M: int, num_sms: int) -> list[int]:
+    """Testing aid (host only, see pn_tc_split): the unit ranges the
+    tensor-core GEMV would give its thread blocks for tensors ``shapes`` =
+    [(pn_type, N, K), ...] at M tokens on num_sms SMs; returns starts, with
+    block c taking units [starts[c], starts[c + 1])."""
+    shapes = list(shapes)
+    n = len(shapes)
+    types = (ctypes.c_int * n)(*[s[0] for s in shapes])
+    Ns = (ctypes.c_int64 * n)(*[s[1] for s in shapes])
+    Ks = (ctypes.c_int64 * n)(*[s[2] for s in shapes])
+    starts = (ctypes.c_uint32 * (max(num_sms, 1) + 1))()
+    grid = ctypes.c_int(0)
+    _check(lib().pn_tc_split(types, Ns, Ks, n, M, num_sms, starts, ctypes.byref(grid)), "pn_tc_split")
+    return list(starts[: grid.value + 1])

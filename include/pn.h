@@ -284,6 +284,23 @@ void pn_set_wait_timeout_ns(uint64_t ns);
  */
 void pn_set_test_stall(int on);
 
+/*
+ * Testing aid (host only; needs no device): the work split the tensor-core
+ * GEMV kernel for 3 <= M <= 16 would use for a pn_gemv_layer call on
+ * tensors of these types and shapes on a GPU with num_sms SMs.  types, N
+ * and K are host arrays of `count` (1 .. PN_MAX_LAYER) entries; every N >= 1
+ * and every K a positive multiple of 8 blocks (640 for pn3t, 512 for pn4t),
+ * else PN_EINVAL.  Units are numbered over the tensors in order, each
+ * tensor's 16-row tiles in turn and each tile's 8-block chunks within it.
+ * On PN_OK, *grid is the number of thread blocks and block c takes units
+ * [starts[c], starts[c + 1]) (starts: host array of at least num_sms + 1
+ * entries; starts[0] = 0, starts[*grid] = all units).  Every range holds at
+ * least one whole tile's units, so a tile has at most two owners; the split
+ * depends only on the arguments.
+ */
+pn_status pn_tc_split(const int* types, const int64_t* N, const int64_t* K, int count, int M, int num_sms,
+                      uint32_t* starts, int* grid);
+
 #ifdef __cplusplus
 }
 #endif
