@@ -26,6 +26,11 @@
 // 32 (pn4t) MMAs.  Each column's sum is scaled by its own block scale d and
 // the columns of one token are then added.
 //
+// Staging.  Each warp streams its units through a private two-stage ring:
+// per unit, one 2-D TMA box of weights (15 rows x 272 bytes) and one bulk
+// copy per token of the chunk's fp16 activations land in the same stage on
+// one mbarrier, so both the codes and x are read from shared memory.
+//
 // Work split.  A unit is a 15-row tile x one 8-block chunk (272 bytes per
 // row).  Units are numbered tile-major over every tensor of the call; the grid
 // splits them into equal contiguous ranges (see kCostPn3t), each at least one
@@ -68,14 +73,22 @@ constexpr int kBoxBytes = kRows * kChunkBytes;            // 4080
 // slower), so both weigh the same.
 constexpr uint32_t kCostPn3t = 1, kCostPn4t = 1;
 constexpr int kMaxGrid = 512;                             // thread blocks per launch, at most
-constexpr int kStageBytes = 4096;
+constexpr int kStreamMaxM = 2;                            // tokens this kernel serves
+// A stage holds one unit's weight box and its activation chunk for each
+// token (token m at kXOffset + m * kXTokenBytes; a pn3t chunk is 640 fp16,
+// a pn4t chunk 512), all copied on the stage's mbarrier, so the decode reads
+// x from shared memory like the weights.
+constexpr int kXOffset = 4096;
+constexpr int kXTokenBytes = kChunkBlocks * 80 * 2;       // 1280
+constexpr int kStageBytes = kXOffset + kStreamMaxM * kXTokenBytes;   // 6656
 constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 // The all-ones code rows (pn3t, pn4t) stand in for row 15 of every stage; they
 // sit at the bank offset row 15 would have (15 * 272 = 112 mod 128).
 constexpr int kOnesOffset = kRingBytes + 112;
 constexpr int kOnesBytes = 2 * kChunkBytes + 16;          // + slack for realigning loads
-constexpr int kPartOffset = (kOnesOffset + kOnesBytes + 15) / 16 * 16;
-constexpr int kStreamMaxM = 2;                            // tokens this kernel serves
+constexpr int kZeroOffset = (kOnesOffset + kOnesBytes + 15) / 16 * 16;
+constexpr int kZeroBytes = 256;                           // zeros read by lanes with an empty B fragment
+constexpr int kPartOffset = kZeroOffset + kZeroBytes;
 constexpr int kSlotFloats = 16 * kStreamMaxM;             // [row][token]
 constexpr int kPartBytes = kWarps * 2 * kSlotFloats * 4;
 constexpr int kCntOffset = kPartOffset + kPartBytes;
@@ -84,12 +97,9 @@ constexpr int kSmemBytes = kBarOffset + kWarps * kStages * 8;
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                    // PN_ETIMEOUT
 
-static_assert(kBoxBytes <= kStageBytes && kStageBytes % 128 == 0, "stages stay TMA-aligned");
+static_assert(kBoxBytes <= kXOffset && kXOffset % 16 == 0 && kStageBytes % 128 == 0, "stages stay TMA-aligned");
 static_assert(kSmemBytes <= 113 * 1024, "two thread blocks fit on one SM");
 static_assert(kBarOffset % 8 == 0, "aligned barriers");
-
-// Zeros read by the lanes whose B fragment is empty (at most 40 code pairs).
-__device__ __align__(16) uint32_t g_zero_pairs[64];
 
 struct STensor {
     const uint16_t* x;
@@ -214,25 +224,15 @@ struct Acc {
     }
 };
 
-// NP consecutive code-pair activations (fp16 pairs) from p, which is aligned
-// to ALIGN bytes.  Read through the non-coherent path (x is read-only here).
-template <int NP, int ALIGN>
-__device__ __forceinline__ void load_pairs(const uint32_t* p, uint32_t (&v)[NP]) {
-    if constexpr (ALIGN >= 16 && NP % 4 == 0) {
+// NP consecutive code-pair activations (fp16 pairs) from the staged chunk
+// at p (shared memory, 16-byte aligned; NP a multiple of 4).
+template <int NP>
+__device__ __forceinline__ void load_pairs(const uint8_t* p, uint32_t (&v)[NP]) {
+    static_assert(NP % 4 == 0, "16-byte loads");
 #pragma unroll
-        for (int i = 0; i < NP / 4; ++i) {
-            const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + i);
-            v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
-        }
-    } else if constexpr (ALIGN >= 8 && NP % 2 == 0) {
-#pragma unroll
-        for (int i = 0; i < NP / 2; ++i) {
-            const uint2 q = __ldg(reinterpret_cast<const uint2*>(p) + i);
-            v[2 * i] = q.x; v[2 * i + 1] = q.y;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < NP; ++i) v[i] = __ldg(p + i);
+    for (int i = 0; i < NP / 4; ++i) {
+        const uint4 q = *reinterpret_cast<const uint4*>(p + 16 * i);
+        v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
     }
 }
 
@@ -256,29 +256,29 @@ struct Lane {
     int g, t;
     const uint8_t* r0;     // staged row g
     const uint8_t* r1;     // staged row g + 8, or the all-ones row for g = 7
+    const uint8_t* x;      // staged activations of token 0 (token m at + m * kXTokenBytes)
+    const uint8_t* zeros;  // kZeroBytes of zeros
 };
 
 // ---------------------------------------------------------------------------
 // One unit (15 rows + ones row, 8 blocks), Mp = 8 / BPM tokens.  Adds the
 // lane's scaled sums to acc: BPM 8 / 4 / 2: acc[h] = row g + 8h of token
 // tok(t); BPM 1: acc[2h + j] = row g + 8h of token 2t + j.
-// xc: the chunk's activations of token 0 (token stride K).
 // ---------------------------------------------------------------------------
 
 template <int TYPE>
-__device__ __forceinline__ void unit_b8(const Lane& L, const uint16_t* xc, int K, int M, float (&acc)[4]) {
+__device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4]) {
     using F = Format<TYPE>;
     constexpr int kP = F::kPairs;
     const int g = L.g, t = L.t;
-    (void)K; (void)M;
+    (void)M;
     // k-pair t <-> odd block 2t+1, k-pair t+4 <-> even block 2t; step s of
     // the unit takes code pair s % kP of word s / kP of both blocks.  The
     // B columns are the blocks: lane g == 2t+1 carries block 2t+1's
     // activations in b0, lane g == 2t block 2t's in b1, every other B
     // register is zero.
-    const uint32_t* xo = (g == 2 * t + 1) ? reinterpret_cast<const uint32_t*>(xc + (2 * t + 1) * F::kPerBlock)
-                                          : g_zero_pairs;
-    const uint32_t* xe = (g == 2 * t) ? reinterpret_cast<const uint32_t*>(xc + 2 * t * F::kPerBlock) : g_zero_pairs;
+    const uint8_t* xo = (g == 2 * t + 1) ? L.x + (2 * t + 1) * F::kPerBlock * 2 : L.zeros;
+    const uint8_t* xe = (g == 2 * t) ? L.x + 2 * t * F::kPerBlock * 2 : L.zeros;
     // block 2t starts 4-byte aligned in a staged row: aligned word v[i] at
     // byte 4i holds (previous half, next half); its words are realigned with
     // one byte permute, and v[0] / v[8] also hold the two blocks' scales
@@ -313,8 +313,8 @@ __device__ __forceinline__ void unit_b8(const Lane& L, const uint16_t* xc, int K
     static_for<2 * kP>([&](auto qc) {
         constexpr int Q = decltype(qc)::value;          // four steps per 16-byte activation load
         uint32_t bo[4], be[4];
-        load_pairs<4, 16>(xo + 4 * Q, bo);
-        load_pairs<4, 16>(xe + 4 * Q, be);
+        load_pairs<4>(xo + 16 * Q, bo);
+        load_pairs<4>(xe + 16 * Q, be);
         static_for<4>([&](auto jc) {
             constexpr int S = 4 * Q + decltype(jc)::value;
             constexpr int W = S / kP, Pp = S % kP;
@@ -346,7 +346,7 @@ __device__ __forceinline__ void unit_b8(const Lane& L, const uint16_t* xc, int K
 }
 
 template <int TYPE>
-__device__ __forceinline__ void unit_b4(const Lane& L, const uint16_t* xc, int K, int M, float (&acc)[4]) {
+__device__ __forceinline__ void unit_b4(const Lane& L, int M, float (&acc)[4]) {
     using F = Format<TYPE>;
     constexpr int kP = F::kPairs;
     constexpr int kSteps = 4 * kP;                 // per group of 4 blocks
@@ -354,17 +354,17 @@ __device__ __forceinline__ void unit_b4(const Lane& L, const uint16_t* xc, int K
     const uint32_t sel = (t & 1) ? 0x3210u : 0x5432u;
     // column c <-> token c >> 2, block c & 3 of the group; lane t decodes block t
     const bool has_b = (g & 3) == t && (g >> 2) < M;
-    const uint16_t* xt = xc + static_cast<int64_t>(g >> 2) * K;
+    const uint8_t* xt = L.x + (g >> 2) * kXTokenBytes;
     static_for<2>([&](auto gc) {
         constexpr int G = decltype(gc)::value;
         const int blk = 4 * G + t;
         uint32_t w[2][8];
         load_words_rt<8>(L.r0, blk, 0, sel, w[0]);
         load_words_rt<8>(L.r1, blk, 0, sel, w[1]);
-        const uint32_t* xb = has_b ? reinterpret_cast<const uint32_t*>(xt + blk * F::kPerBlock) : g_zero_pairs;
+        const uint8_t* xb = has_b ? xt + blk * F::kPerBlock * 2 : L.zeros;
         uint32_t b0[kSteps], b1[kSteps];
-        load_pairs<kSteps, 16>(xb, b0);                                  // words 0..3
-        load_pairs<kSteps, 16>(has_b ? xb + kSteps : g_zero_pairs, b1);  // words 4..7
+        load_pairs<kSteps>(xb, b0);                                      // words 0..3
+        load_pairs<kSteps>(has_b ? xb + 4 * kSteps : L.zeros, b1);       // words 4..7
         Acc<TYPE> A;
         A.zero();
         static_for<kSteps>([&](auto sc) {
@@ -398,9 +398,9 @@ __device__ __forceinline__ void unit_b4(const Lane& L, const uint16_t* xc, int K
 }
 
 template <int BPM, int TYPE>
-__device__ __forceinline__ void unit(const Lane& L, const uint16_t* xc, int K, int M, float (&acc)[4]) {
-    if constexpr (BPM == 8) unit_b8<TYPE>(L, xc, K, M, acc);
-    else unit_b4<TYPE>(L, xc, K, M, acc);
+__device__ __forceinline__ void unit(const Lane& L, int M, float (&acc)[4]) {
+    if constexpr (BPM == 8) unit_b8<TYPE>(L, M, acc);
+    else unit_b4<TYPE>(L, M, acc);
 }
 
 // ------------------------------------------------------------ tile results --
@@ -554,11 +554,24 @@ struct Ring {
     uint32_t done = 0, issued = 0;
 };
 
+// Lane 0: the copies of unit c into stage `dst` (shared address), completing
+// on `bar`: the weight box and the chunk's activations of every token.  With
+// `copy` false the bytes are announced but nothing is copied (testing aid).
+__device__ __forceinline__ void issue_unit(const SParams& P, uint32_t dst, uint32_t bar, const Cursor& c, bool copy) {
+    const STensor& T = P.t[c.e];
+    const int halves = kChunkBlocks * per_block(T.type);
+    mbar_arrive_expect_tx(bar, kBoxBytes + P.M * halves * 2);
+    if (!copy) return;
+    tma_load_2d(dst, &P.wmap[c.e], c.chunk * kBoxWords, c.tile * kRows, bar);
+    const uint16_t* x = T.x + static_cast<int64_t>(c.chunk) * halves;
+    for (int m = 0; m < P.M; ++m)
+        bulk_g2s(dst + kXOffset + m * kXTokenBytes, x + static_cast<int64_t>(m) * T.K, halves * 2, bar);
+}
+
 template <int BPM, int TYPE>
-__device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, Lane& L, const uint16_t* xc, int K,
+__device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, Lane& L,
                           uint32_t len, uint32_t total, uint32_t nr, uint32_t c0, Ring& R, Issuer& I,
                           float (&acc)[4]) {
-    constexpr int kChunkHalves = kChunkBlocks * Format<TYPE>::kPerBlock;
     const uint32_t ring = smem_addr(smem) + warp * kStages * kStageBytes;
     const uint8_t* ring_p = smem + warp * kStages * kStageBytes;
     const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;
@@ -571,16 +584,14 @@ __device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, L
         const uint8_t* stage = ring_p + R.s * kStageBytes;
         L.r0 = stage + L.g * kChunkBytes;
         L.r1 = L.g == 7 ? ones : stage + (L.g + 8) * kChunkBytes;
-        unit<BPM, TYPE>(L, xc, K, P.M, acc);
-        xc += kChunkHalves;
+        L.x = stage + kXOffset;
+        unit<BPM, TYPE>(L, P.M, acc);
         __syncwarp();
         ++R.done;
         if (R.issued < total) {                   // refill this stage
             if (lane == 0) {
                 fence_proxy_async_smem();
-                const uint32_t bar = bar0 + 8 * R.s;
-                mbar_arrive_expect_tx(bar, kBoxBytes);
-                tma_load_2d(ring + R.s * kStageBytes, &P.wmap[I.c.e], I.c.chunk * kBoxWords, I.c.tile * kRows, bar);
+                issue_unit(P, ring + R.s * kStageBytes, bar0 + 8 * R.s, I.c, true);
             }
             I.advance(P, nr, c0);
             ++R.issued;
@@ -626,14 +637,9 @@ __device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, ui
 
     Ring R;
     for (int s = 0; s < kStages && R.issued < total; ++s) {
-        if (lane == 0) {
-            const uint32_t bar = bar0 + 8 * s;
-            mbar_arrive_expect_tx(bar, kBoxBytes);
-            // (testing aid: with stall_first_step a warp's first unit is
-            // announced but never copied, so its wait can only time out)
-            if (!(s == 0 && P.stall_first_step))
-                tma_load_2d(ring + s * kStageBytes, &P.wmap[I.c.e], I.c.chunk * kBoxWords, I.c.tile * kRows, bar);
-        }
+        // (testing aid: with stall_first_step a warp's first unit is
+        // announced but never copied, so its wait can only time out)
+        if (lane == 0) issue_unit(P, ring + s * kStageBytes, bar0 + 8 * s, I.c, !(s == 0 && P.stall_first_step));
         I.advance(P, nr, c0);
         ++R.issued;
     }
@@ -641,6 +647,7 @@ __device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, ui
     Lane L;
     L.g = lane >> 2;
     L.t = lane & 3;
+    L.zeros = smem + kZeroOffset;
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     uint32_t q = p0;
     Cursor cur{0, 0, 0};
@@ -651,9 +658,8 @@ __device__ void run_warp(const SParams& P, uint8_t* smem, int warp, int lane, ui
         const uint32_t run_end = q < nr ? (nr < p1 ? nr : p1) : p1;
         const uint32_t room = static_cast<uint32_t>(T.chunks - cur.chunk);
         const uint32_t len = run_end - q < room ? run_end - q : room;
-        const uint16_t* xc = T.x + cur.chunk * kChunkBlocks * per_block(T.type);
-        ok = T.type == kPn3t ? part_loop<BPM, kPn3t>(P, smem, warp, lane, L, xc, T.K, len, total, nr, c0, R, I, acc)
-                             : part_loop<BPM, kPn4t>(P, smem, warp, lane, L, xc, T.K, len, total, nr, c0, R, I, acc);
+        ok = T.type == kPn3t ? part_loop<BPM, kPn3t>(P, smem, warp, lane, L, len, total, nr, c0, R, I, acc)
+                             : part_loop<BPM, kPn4t>(P, smem, warp, lane, L, len, total, nr, c0, R, I, acc);
         if (!ok) break;
         // this warp's part of tile cur.tile ends here
         const uint32_t tbeg = T.unit_base + static_cast<uint32_t>(cur.tile) * T.chunks;
@@ -712,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const __grid_c
         }
         reinterpret_cast<uint16_t*>(smem + kOnesOffset)[i] = v;
     }
+    for (int i = threadIdx.x; i < kZeroBytes / 4; i += kThreads) reinterpret_cast<uint32_t*>(smem + kZeroOffset)[i] = 0u;
     if (lane == 0) {
         const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;
         for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
