@@ -70,7 +70,10 @@ constexpr int kBoxBytes = kRows * kChunkBytes;            // 4080
 // the thread blocks.  This kernel's time follows its memory stream more than
 // its decode: on a mixed pn3t / pn4t layer an even split of the bytes measured
 // fastest (weighting pn3t units 1.07 to 1.25 times a pn4t unit was 3 to 7 %
-// slower), so both weigh the same.
+// slower), so both weigh the same.  Re-measured with x staged in shared
+// memory on the 27B-class layer: 9 / 8 within 0.4 % of even at one token,
+// 5 / 4 and every pn4t-heavier weight slower (up to 10 %); at two tokens 8 / 9
+// was 2 % faster but 5 % slower at one token.
 constexpr uint32_t kCostPn3t = 1, kCostPn4t = 1;
 constexpr int kMaxGrid = 512;                             // thread blocks per launch, at most
 constexpr int kStreamMaxM = 2;                            // tokens this kernel serves
