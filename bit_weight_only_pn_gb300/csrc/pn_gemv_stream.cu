@@ -8,15 +8,12 @@
 // (v100-skinny README, "How QPN works"), with exact products and fp32 sums.
 //
 // Decode.  A code pair (one code in each 16-bit half of a word, at the same
-// offset, "Codes never straddle the two halves of a word") is masked in place
-// with one AND.  Each half then holds n * 2^off as an fp16 bit pattern with a
-// zero exponent field: the fp16 subnormal n * 2^(off - 24), exactly.  These
-// halves are the A operand of mma.sync m16n8k16 (fp16 in, fp32 accumulate), so
-// the tensor cores form sum_k n_k x_k exactly per product, one accumulator per
-// code offset; the offsets are folded with power-of-two factors afterwards.
-// The zero point comes from the same MMAs: a tile holds 15 weight rows and a
-// 16th row whose codes are all 1, which yields sum_k x_k over exactly the same
-// k-slots, and each weight row's block sum is sum n x - z sum x.
+// offset, "Codes never straddle the two halves of a word") becomes the exact
+// half2 (n - z, n' - z) with one LOP3 and one HFMA2 (decode_pair), which is
+// an A-fragment register of mma.sync m16n8k16 (fp16 in, fp32 accumulate).
+// The zero point is taken off every code before the multiply, so a weight on
+// the zero code ("Zero is a code, and the scale has a sign") contributes an
+// exact 0 and carries no rounding error, whatever its activation.
 //
 // Fragment mapping.  An MMA covers 8 blocks (M = 1) or 4 blocks (M = 2): its
 // eight k-pairs are shared out between those blocks and its eight columns are
@@ -27,11 +24,11 @@
 // the columns of one token are then added.
 //
 // Staging.  Each warp streams its units through a private two-stage ring:
-// per unit, one 2-D TMA box of weights (15 rows x 272 bytes) and one bulk
+// per unit, one 2-D TMA box of weights (16 rows x 272 bytes) and one bulk
 // copy per token of the chunk's fp16 activations land in the same stage on
 // one mbarrier, so both the codes and x are read from shared memory.
 //
-// Work split.  A unit is a 15-row tile x one 8-block chunk (272 bytes per
+// Work split.  A unit is a 16-row tile x one 8-block chunk (272 bytes per
 // row).  Units are numbered tile-major over every tensor of the call; the grid
 // splits them into equal contiguous ranges (see kCostPn3t), each at least one
 // tile long, and the eight warps of a block split the block's range again.  A warp's whole tiles
@@ -61,11 +58,11 @@ constexpr int kThreads = kWarps * 32;
 // with three) measured 3 to 5 % faster than three.  Not through a larger L1:
 // forcing the largest shared-memory carve-out measured the same.
 constexpr int kStages = 2;
-constexpr int kRows = 15;                                 // weight rows per tile
+constexpr int kRows = 16;                                 // weight rows per tile
 constexpr int kChunkBlocks = 8;
 constexpr int kChunkBytes = kChunkBlocks * kBlockBytes;   // 272
 constexpr int kBoxWords = kChunkBytes / 4;                // 68
-constexpr int kBoxBytes = kRows * kChunkBytes;            // 4080
+constexpr int kBoxBytes = kRows * kChunkBytes;            // 4352
 // Relative cost of one unit, pn3t / pn4t, for the split of the units over
 // the thread blocks.  This kernel's time follows its memory stream more than
 // its decode: on a mixed pn3t / pn4t layer an even split of the bytes measured
@@ -81,15 +78,11 @@ constexpr int kStreamMaxM = 2;                            // tokens this kernel 
 // token (token m at kXOffset + m * kXTokenBytes; a pn3t chunk is 640 fp16,
 // a pn4t chunk 512), all copied on the stage's mbarrier, so the decode reads
 // x from shared memory like the weights.
-constexpr int kXOffset = 4096;
+constexpr int kXOffset = kBoxBytes;
 constexpr int kXTokenBytes = kChunkBlocks * 80 * 2;       // 1280
-constexpr int kStageBytes = kXOffset + kStreamMaxM * kXTokenBytes;   // 6656
+constexpr int kStageBytes = kXOffset + kStreamMaxM * kXTokenBytes;   // 6912
 constexpr int kRingBytes = kWarps * kStages * kStageBytes;
-// The all-ones code rows (pn3t, pn4t) stand in for row 15 of every stage; they
-// sit at the bank offset row 15 would have (15 * 272 = 112 mod 128).
-constexpr int kOnesOffset = kRingBytes + 112;
-constexpr int kOnesBytes = 2 * kChunkBytes + 16;          // + slack for realigning loads
-constexpr int kZeroOffset = (kOnesOffset + kOnesBytes + 15) / 16 * 16;
+constexpr int kZeroOffset = kRingBytes;
 constexpr int kZeroBytes = 256;                           // zeros read by lanes with an empty B fragment
 constexpr int kPartOffset = kZeroOffset + kZeroBytes;
 constexpr int kSlotFloats = 16 * kStreamMaxM;             // [row][token]
@@ -102,6 +95,7 @@ constexpr uint32_t kStatusTimeout = 5;                    // PN_ETIMEOUT
 
 static_assert(kBoxBytes <= kXOffset && kXOffset % 16 == 0 && kStageBytes % 128 == 0, "stages stay TMA-aligned");
 static_assert(kSmemBytes <= 113 * 1024, "two thread blocks fit on one SM");
+static_assert(kXOffset % 128 == 0, "activation chunks stay 16-byte aligned");
 static_assert(kBarOffset % 8 == 0, "aligned barriers");
 
 struct STensor {
@@ -190,41 +184,18 @@ __device__ __forceinline__ void mma_acc(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Code pair P of a word, masked in place (see the header): both halves become
-// the fp16 subnormals n * 2^(off - 24).  `sh` is the word shifted right by the
-// format's high shift, which brings the upper pairs into the mantissa field.
-template <int TYPE, int P>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t sh) {
-    using F = Format<TYPE>;
-    constexpr bool kHigh = P >= F::kLowPairs;
-    constexpr int kOff = F::kBits * (kHigh ? P - F::kLowPairs : P);
-    constexpr uint32_t kMask = ((1u << F::kBits) - 1u) << kOff;
-    return (kHigh ? sh : w) & (kMask | (kMask << 16));
-}
-
-// Accumulator class of code pair P: its offset / bits (pn3t 0, 1, 2; pn4t 0, 1).
-template <int TYPE, int P>
-__host__ __device__ constexpr int pair_class() {
-    using F = Format<TYPE>;
-    return P >= F::kLowPairs ? P - F::kLowPairs : P;
-}
-
-template <int TYPE>
-struct Acc {
-    static constexpr int kClasses = TYPE == kPn3t ? 3 : 2;
-    float c[kClasses][4];
+// Four accumulators per lane: consecutive MMAs of a unit go to different
+// ones, so a chain of dependent MMAs is a quarter of the unit long.
+struct Acc4 {
+    float c[4][4];
     __device__ __forceinline__ void zero() {
 #pragma unroll
-        for (int k = 0; k < kClasses; ++k)
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int i = 0; i < 4; ++i) c[k][i] = 0.0f;
     }
-    // sum over classes with the classes' power-of-two weights, in units of
-    // 2^-24 (every product carries that factor)
-    __device__ __forceinline__ float fold(int i) const {
-        if constexpr (TYPE == kPn3t) return fmaf(c[2][i], 0.015625f, fmaf(c[1][i], 0.125f, c[0][i]));
-        else return fmaf(c[1][i], 0.0625f, c[0][i]);
-    }
+    // (c0 + c1) + (c2 + c3): a fixed tree
+    __device__ __forceinline__ float sum(int i) const { return (c[0][i] + c[1][i]) + (c[2][i] + c[3][i]); }
 };
 
 // NP consecutive code-pair activations (fp16 pairs) from the staged chunk
@@ -258,15 +229,14 @@ __device__ __forceinline__ float lds_half(const uint8_t* p) { return __half2floa
 struct Lane {
     int g, t;
     const uint8_t* r0;     // staged row g
-    const uint8_t* r1;     // staged row g + 8, or the all-ones row for g = 7
+    const uint8_t* r1;     // staged row g + 8
     const uint8_t* x;      // staged activations of token 0 (token m at + m * kXTokenBytes)
     const uint8_t* zeros;  // kZeroBytes of zeros
 };
 
 // ---------------------------------------------------------------------------
-// One unit (15 rows + ones row, 8 blocks), Mp = 8 / BPM tokens.  Adds the
-// lane's scaled sums to acc: BPM 8 / 4 / 2: acc[h] = row g + 8h of token
-// tok(t); BPM 1: acc[2h + j] = row g + 8h of token 2t + j.
+// One unit (16 rows, 8 blocks), Mp = 8 / BPM tokens.  Adds the lane's scaled
+// sums to acc: acc[h] = row g + 8h of token tok(t).
 // ---------------------------------------------------------------------------
 
 template <int TYPE>
@@ -304,14 +274,12 @@ __device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4]) {
             wo0[i] = lds_u32(e0 + 36 + 4 * i);
             wo1[i] = lds_u32(e1 + 36 + 4 * i);
         }
-        v0 = a0[0];
-        v1 = a1[0];
-        d_e0 = half_lo(v0);
-        d_e1 = half_lo(v1);
+        d_e0 = half_lo(a0[0]);
+        d_e1 = half_lo(a1[0]);
         v0 = a0[8];
         v1 = a1[8];
     }
-    Acc<TYPE> A;
+    Acc4 A;
     A.zero();
     static_for<2 * kP>([&](auto qc) {
         constexpr int Q = decltype(qc)::value;          // four steps per 16-byte activation load
@@ -323,23 +291,17 @@ __device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4]) {
             constexpr int W = S / kP, Pp = S % kP;
             const uint32_t so0 = wo0[W] >> F::kHighShift, so1 = wo1[W] >> F::kHighShift;
             const uint32_t se0 = we0[W] >> F::kHighShift, se1 = we1[W] >> F::kHighShift;
-            mma_acc(A.c[pair_class<TYPE, Pp>()],
-                    code_pair<TYPE, Pp>(wo0[W], so0), code_pair<TYPE, Pp>(wo1[W], so1),
-                    code_pair<TYPE, Pp>(we0[W], se0), code_pair<TYPE, Pp>(we1[W], se1), bo[S % 4], be[S % 4]);
+            mma_acc(A.c[S & 3],
+                    decode_pair<TYPE, Pp>(wo0[W], so0), decode_pair<TYPE, Pp>(wo1[W], so1),
+                    decode_pair<TYPE, Pp>(we0[W], se0), decode_pair<TYPE, Pp>(we1[W], se1), bo[S % 4], be[S % 4]);
         });
     });
     const float d_o0 = half_hi(v0), d_o1 = half_hi(v1);        // v[8]: the odd block's scale
-    // column 2t <-> block 2t (even), 2t+1 <-> block 2t+1 (odd); row 15 = sums of x
-    float u[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) u[i] = A.fold(i);
-    const float s_e = __shfl_sync(0xFFFFFFFFu, u[2], 28 + t);
-    const float s_o = __shfl_sync(0xFFFFFFFFu, u[3], 28 + t);
-    constexpr float kNegZ = -static_cast<float>(F::kZero);
-    float r0 = d_e0 * fmaf(s_e, kNegZ, u[0]);
-    r0 = fmaf(d_o0, fmaf(s_o, kNegZ, u[1]), r0);
-    float r1 = d_e1 * fmaf(s_e, kNegZ, u[2]);
-    r1 = fmaf(d_o1, fmaf(s_o, kNegZ, u[3]), r1);
+    // column 2t <-> block 2t (even), 2t+1 <-> block 2t+1 (odd)
+    float r0 = d_e0 * A.sum(0);
+    r0 = fmaf(d_o0, A.sum(1), r0);
+    float r1 = d_e1 * A.sum(2);
+    r1 = fmaf(d_o1, A.sum(3), r1);
     r0 += __shfl_xor_sync(0xFFFFFFFFu, r0, 1);
     r1 += __shfl_xor_sync(0xFFFFFFFFu, r1, 1);
     r0 += __shfl_xor_sync(0xFFFFFFFFu, r0, 2);
@@ -368,32 +330,26 @@ __device__ __forceinline__ void unit_b4(const Lane& L, int M, float (&acc)[4]) {
         uint32_t b0[kSteps], b1[kSteps];
         load_pairs<kSteps>(xb, b0);                                      // words 0..3
         load_pairs<kSteps>(has_b ? xb + 4 * kSteps : L.zeros, b1);       // words 4..7
-        Acc<TYPE> A;
+        Acc4 A;
         A.zero();
         static_for<kSteps>([&](auto sc) {
             constexpr int S = decltype(sc)::value;
             constexpr int W = S / kP, P = S % kP;
             const uint32_t s00 = w[0][W] >> F::kHighShift, s10 = w[1][W] >> F::kHighShift;
             const uint32_t s01 = w[0][W + 4] >> F::kHighShift, s11 = w[1][W + 4] >> F::kHighShift;
-            mma_acc(A.c[pair_class<TYPE, P>()],
-                    code_pair<TYPE, P>(w[0][W], s00), code_pair<TYPE, P>(w[1][W], s10),
-                    code_pair<TYPE, P>(w[0][W + 4], s01), code_pair<TYPE, P>(w[1][W + 4], s11),
+            mma_acc(A.c[S & 3],
+                    decode_pair<TYPE, P>(w[0][W], s00), decode_pair<TYPE, P>(w[1][W], s10),
+                    decode_pair<TYPE, P>(w[0][W + 4], s01), decode_pair<TYPE, P>(w[1][W + 4], s11),
                     b0[S], b1[S]);
         });
-        float u[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) u[i] = A.fold(i);
-        const float s0 = __shfl_sync(0xFFFFFFFFu, u[2], 28 + t);
-        const float s1 = __shfl_sync(0xFFFFFFFFu, u[3], 28 + t);
         // lane columns 2t, 2t+1 <-> token t >> 1, blocks 4G + 2(t & 1) + {0, 1}
         const int bb = 4 * G + 2 * (t & 1);
-        constexpr float kNegZ = -static_cast<float>(F::kZero);
         float v[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const uint8_t* r = h ? L.r1 : L.r0;
             const float d0 = lds_half(r + kBlockBytes * bb), d1 = lds_half(r + kBlockBytes * (bb + 1));
-            v[h] = fmaf(d1, fmaf(s1, kNegZ, u[2 * h + 1]), d0 * fmaf(s0, kNegZ, u[2 * h]));
+            v[h] = fmaf(d1, A.sum(2 * h + 1), d0 * A.sum(2 * h));
             v[h] += __shfl_xor_sync(0xFFFFFFFFu, v[h], 1);
             acc[h] += v[h];
         }
@@ -438,7 +394,7 @@ __device__ __forceinline__ void store_tile(const SParams& P, const Cursor& c, in
         int row, tok;
         if (!acc_slot<BPM>(g, t, i, row, tok)) continue;
         const int r = c.tile * kRows + row;
-        if (r < T.N && tok < P.M) T.y[static_cast<int64_t>(tok) * T.N + r] = acc[i] * 16777216.0f;   // x 2^24
+        if (r < T.N && tok < P.M) T.y[static_cast<int64_t>(tok) * T.N + r] = acc[i];
     }
 }
 
@@ -521,7 +477,7 @@ __device__ __forceinline__ void exchange(const SParams& P, const Cursor& c, int 
         const float other = __uint_as_float(static_cast<uint32_t>(got));
         const float v = first ? acc[i] + other : other + acc[i];     // first chunks + later chunks
         const int r = c.tile * kRows + row;
-        if (r < T.N) T.y[static_cast<int64_t>(tok) * T.N + r] = v * 16777216.0f;    // x 2^24
+        if (r < T.N) T.y[static_cast<int64_t>(tok) * T.N + r] = v;
         st_relaxed_u64(w, 0ull);
     }
 }
@@ -578,7 +534,6 @@ __device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, L
     const uint32_t ring = smem_addr(smem) + warp * kStages * kStageBytes;
     const uint8_t* ring_p = smem + warp * kStages * kStageBytes;
     const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;
-    const uint8_t* ones = smem + kOnesOffset + (TYPE == kPn3t ? 0 : kChunkBytes);
     for (uint32_t k = 0; k < len; ++k) {
         if (!warp_wait(bar0 + 8 * R.s, R.phase, P.timeout_ns, lane)) {
             if (lane == 0) atomicCAS(P.status, 0u, kStatusTimeout);
@@ -586,7 +541,7 @@ __device__ bool part_loop(const SParams& P, uint8_t* smem, int warp, int lane, L
         }
         const uint8_t* stage = ring_p + R.s * kStageBytes;
         L.r0 = stage + L.g * kChunkBytes;
-        L.r1 = L.g == 7 ? ones : stage + (L.g + 8) * kChunkBytes;
+        L.r1 = stage + (L.g + 8) * kChunkBytes;
         L.x = stage + kXOffset;
         unit<BPM, TYPE>(L, P.M, acc);
         __syncwarp();
@@ -710,17 +665,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const __grid_c
     griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t c0 = range_start(P, blockIdx.x), c1 = range_start(P, blockIdx.x + 1);
-    // all-ones code rows: pn3t (codes 1 at 0, 3, 6, 9, 12 of each half), pn4t
-    // (1 in every nibble); scales 0
-    for (int i = threadIdx.x; i < kOnesBytes / 2; i += kThreads) {
-        uint16_t v = 0;
-        if (i < 2 * (kChunkBytes / 2)) {
-            const int row = i / (kChunkBytes / 2), hw = i % (kChunkBytes / 2);   // half-word in the row
-            const int inblk = hw % (kBlockBytes / 2);
-            if (inblk != 0) v = row == 0 ? 0x1249u : 0x1111u;
-        }
-        reinterpret_cast<uint16_t*>(smem + kOnesOffset)[i] = v;
-    }
     for (int i = threadIdx.x; i < kZeroBytes / 4; i += kThreads) reinterpret_cast<uint32_t*>(smem + kZeroOffset)[i] = 0u;
     if (lane == 0) {
         const uint32_t bar0 = smem_addr(smem + kBarOffset) + warp * kStages * 8;

@@ -117,3 +117,47 @@ def sylvester_hadamard(n: int) -> np.ndarray:
     while h.shape[0] < n:
         h = np.block([[h, h], [h, -h]])
     return h
+
+
+def zero_code_case(rng: np.random.Generator, pn_type: int, n_rows: int, n_blocks: int, M: int,
+                   scale_exp=(-14, 3), tiny=1e-4, big=1e3):
+    """Weights dominated by the zero code, with activations that punish any
+    computation which does not subtract the zero point code by code.
+
+    Format page, "Zero is a code, and the scale has a sign": n = z decodes to
+    an exact zero.  In every block a few positions S_b (the same for all rows)
+    hold the only non-zero steps: the first is the full-range step q = -z (so
+    the block's scale is exactly d), the others random in [-z, z-1].  Every
+    other code is n = z (weight 0).  x is tiny (about ``tiny``) at S_b and
+    large (up to ``big``, random sign) everywhere else, so the exact outputs
+    are small while sum_k |x_k| over a block is large: a kernel that forms
+    sum n*x - z*sum x loses the answer to rounding, one that multiplies
+    exact (n - z) values does not.  Scales d have random sign, 10-bit
+    mantissa and exponent in ``scale_exp`` (|d| from 2^-14 to about 8 with the
+    default); a few rows get fp16-subnormal scales.  Returns (w fp32 [N][K],
+    x fp16 [M][K]); the weights sit on their grid, so the packer reproduces d
+    and q exactly.
+    """
+    bpb, _, _, z = GEOMETRY[pn_type]
+    K = n_blocks * bpb
+    x = np.empty((M, K), dtype=np.float64)
+    sign = rng.choice([-1.0, 1.0], size=(M, K))
+    x[:] = sign * rng.uniform(1.0, big, size=(M, K))
+    q = np.zeros((n_rows, K), dtype=np.int64)
+    for b in range(n_blocks):
+        s = int(rng.integers(1, 4))
+        pos = b * bpb + rng.choice(bpb, size=s, replace=False)
+        x[:, pos] = rng.choice([-1.0, 1.0], size=(M, s)) * rng.uniform(0.5, 1.5, size=(M, s)) * tiny
+        q[:, pos[0]] = -z
+        if s > 1:
+            q[:, pos[1:]] = rng.integers(-z, z, size=(n_rows, s - 1))
+    e = rng.integers(scale_exp[0], scale_exp[1], size=(n_rows, n_blocks))
+    mant = rng.integers(0, 1024, size=(n_rows, n_blocks))
+    dsign = rng.choice([-1.0, 1.0], size=(n_rows, n_blocks))
+    d = dsign * (1.0 + mant / 1024.0) * np.exp2(e.astype(np.float64))
+    sub = rng.random(n_rows) < 0.05
+    d[sub] = dsign[sub] * rng.integers(1, 1024, size=(int(sub.sum()), n_blocks)) * 2.0 ** -24
+    d = d.astype(np.float16).astype(np.float64)
+    w = (np.repeat(d, bpb, axis=1) * q).astype(np.float32)
+    assert np.array_equal(w.astype(np.float64), np.repeat(d, bpb, axis=1) * q)
+    return w, x.astype(np.float16)
