@@ -10,15 +10,19 @@ call at M = 1 / 8 / 16) and ``--config 6``, the prefill path (a 4096-token
 prompt through the pn3t 5120->17408 tensor: fp16 rebuild + tcgen05 GEMM,
 reported in TFLOP/s against the tensor-core roofline).
 
-Timing: weights are resident in HBM; eight copies (more than twice the 129 MB
-L2) are rotated so every step reads its weights from HBM.  Steps are captured
-in a CUDA graph (launch overhead would otherwise exceed a 6 us kernel) and
-timed with CUDA events on the launching stream, after a barrier and a
-synchronize on both sides; the max over ranks is taken.  ``value`` is the
-effective bandwidth: algorithmic bytes per GEMV (packed weights + x + y) over
-the time per GEMV.  ``e2e`` times the same GEMV through the public Python API
-with x copied from pinned host memory and y copied back and synchronised every
-step.  ``cpu_baseline`` times the CPU oracle on a bounded sample of rows.
+Timing: weights are resident in HBM; copies (together more than twice the
+129 MB L2) are rotated so every step reads its weights from HBM.  Steps are
+captured in CUDA graphs (launch overhead would otherwise exceed a 6 us kernel);
+every graph is replayed once and the GPU kept busy with replays for half a
+second before the timed region, which is exactly ``--steps`` steps timed with
+CUDA events on the launching stream, after a barrier and a synchronize on both
+sides; the max over ranks is taken.  ``value`` is the effective bandwidth:
+algorithmic bytes per GEMV (packed weights + x + y) over the time per GEMV.
+The default line also carries ``m8``, the metric's other half: the seven
+GEMVs of the 27B-class layer at M = 8 in one fused call, timed the same way.
+``e2e`` times the same GEMV through the public Python API with x copied from
+pinned host memory and y copied back and synchronised every step.
+``cpu_baseline`` times the CPU oracle on a bounded sample of rows.
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (weak scaling; no collective on the data path).
@@ -62,6 +66,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-m8", action="store_true",
+                    help="leave out the M = 8 layer measurement that the default line carries as 'm8'")
     ap.add_argument("--m", type=int, default=0,
                     help="GEMV workloads: override the token count M (1 .. 16); 0 keeps the workload's")
     ap.add_argument("--hadamard", type=int, default=0,
@@ -177,20 +183,22 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join("profiles", "traffic.json")
+
+
 def recorded_traffic(cfg: int):
     """Per-launch DRAM bytes (read + write) of the workload's timed kernel from
-    the committed ncu summary, if it was taken on that kernel's current
-    sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "pn_gemv_traffic.md")
+    the committed ncu records (profiles/traffic.json), if they were taken on
+    that kernel's current sources (else None)."""
     try:
-        text = open(path).read()
-    except OSError:
+        with open(os.path.join(ROOT, TRAFFIC_FILE)) as fh:
+            records = json.load(fh)["records"]
+    except (OSError, ValueError, KeyError):
         return None
     want = kernel_source_hash(kernel_of(cfg))
-    for m in re.finditer(r"^traffic config=(\d+) kernel=(\S+) bytes_per_launch=(\d+) source=([0-9a-f]+)",
-                         text, re.M):
-        if int(m.group(1)) == cfg and m.group(4) == want:
-            return int(m.group(3))
+    for r in records:
+        if int(r.get("config", -1)) == cfg and r.get("source") == want:
+            return int(r["bytes_per_launch"])
     return None
 
 
@@ -556,16 +564,18 @@ def run_reference_prefill(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, world, rank, local):
+PREHEAT_S = 0.5              # untimed graph replays before every timed region
+
+
+def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
+    """Times one GEMV workload: `args.steps` steps (one fused launch each)
+    after `args.warmup` warm-up steps, every captured graph replayed once and
+    PREHEAT_S seconds of replays before the timed region, which covers exactly
+    `args.steps` steps.  Returns a dict of the figures of the bench line."""
     import torch
-    from bit_weight_only_pn_gb300 import build, pn, synth
-    if rank == 0 or not os.path.exists(pn.LIBRARY):
-        build.build()             # no-op when the library is up to date
-    dist_barrier(world)
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    name, tensors, M = workload(args.config, args.m)
-    default_m = workload(args.config)[2] == M
+    from bit_weight_only_pn_gb300 import pn, synth
+    name, tensors, M = workload(cfg, m_override)
+    default_m = workload(cfg)[2] == M
     algo = {"auto": pn.ALGO_AUTO, "tc": pn.ALGO_TENSOR_CORE, "cuda_core": pn.ALGO_CUDA_CORE}[args.algo]
     step_bytes = algorithmic_bytes(tensors, M)
     wbytes = sum(N * (K // per_block(t)) * 34 for t, K, N in tensors)
@@ -581,11 +591,11 @@ def run_ours(args, world, rank, local):
     x_all = torch.empty(int(x_offs[-1]), dtype=torch.float16, device=dev)
     sets = []
     for e, (t, K, N) in enumerate(tensors):
-        w = torch.from_numpy(synth.weights(synth.weight_seed(args.config, e), N, K)).to(dev)
+        w = torch.from_numpy(synth.weights(synth.weight_seed(cfg, e), N, K)).to(dev)
         W0 = pn.pack(t, w)
         del w
         xs = x_all[int(x_offs[e]):int(x_offs[e + 1])].view(M, K)
-        xs.copy_(torch.from_numpy(synth.activations(synth.x_seed(args.config, e), M, K)))
+        xs.copy_(torch.from_numpy(synth.activations(synth.x_seed(cfg, e), M, K)))
         sets.append((t, K, N, W0, xs))
     # with --hadamard every tensor's GEMV reads a rotated copy of its activations
     xr = [torch.empty_like(xs) for _, _, _, _, xs in sets] if args.hadamard else None
@@ -614,40 +624,54 @@ def run_ours(args, world, rank, local):
 
     # warm up eagerly (also sets the kernel's shared-memory attribute)
     with torch.cuda.stream(stream):
-        for i in range(min(args.warmup, 3 * copies)):
+        for i in range(max(3, min(args.warmup, 3 * copies))):
             step(rot[i % copies])
     torch.cuda.synchronize(dev)
     if ws.status(stream) != 0:
         raise RuntimeError("device-side error during warm-up")
 
-    def capture(n):
+    def capture(n, first=0):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
+            for i in range(first, first + n):
                 step(rot[i % copies])
         return g
 
     nodes = max(1, min(GRAPH_NODES, args.steps))
     g_full = capture(nodes)
     rem = args.steps % nodes
-    g_rem = capture(rem) if rem else None
+    g_rem = capture(rem, nodes) if rem else None
     reps = args.steps // nodes
+    graphs = [g_full] + ([g_rem] if g_rem is not None else [])
 
-    # warm-up steps through the graph
-    wrem = args.warmup
-    with torch.cuda.stream(stream):
-        while wrem >= nodes:
-            g_full.replay()
-            wrem -= nodes
-        for i in range(wrem):
-            step(rot[i % copies])
-    torch.cuda.synchronize(dev)
+    def preheat():
+        """Replays every graph once (its first replay uploads it), the
+        warm-up steps, then graph replays for PREHEAT_S seconds so that clocks
+        and the overlap of back-to-back launches are at steady state."""
+        with torch.cuda.stream(stream):
+            for g in graphs:
+                g.replay()
+            for i in range(args.warmup):
+                step(rot[i % copies])
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < PREHEAT_S:
+            with torch.cuda.stream(stream):
+                for _ in range(4):
+                    g_full.replay()
+            torch.cuda.synchronize(dev)
+            n += 4
+        return (time.perf_counter() - t0) * 1e3, n * nodes
 
-    props = torch.cuda.get_device_properties(local)
+    preheat_ms, preheat_steps = preheat()
+    props = torch.cuda.get_device_properties(dev)
     uuid = getattr(props, "uuid", None)
-    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else dev.index)
     clocks.start()
     time.sleep(0.3)
+    # keep the GPU busy while the sampler starts, then settle it again
+    preheat()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     dist_barrier(world)
@@ -674,13 +698,13 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public API: pinned x in, pinned y out, every step
     e2e = None
-    if args.e2e_steps > 0:
-        xh = torch.cat([torch.from_numpy(synth.activations(synth.x_seed(args.config, e) + 1000, M, K)).reshape(-1)
+    if e2e_steps > 0:
+        xh = torch.cat([torch.from_numpy(synth.activations(synth.x_seed(cfg, e) + 1000, M, K)).reshape(-1)
                         for e, (t, K, N) in enumerate(tensors)]).pin_memory()
         yh = torch.empty(int(y_offs[-1]), dtype=torch.float32).pin_memory()
         h2d = xh.numel() * 2
         d2h = yh.numel() * 4
-        n_e2e = args.e2e_steps
+        n_e2e = e2e_steps
 
         def e2e_step(i):
             x_all.copy_(xh, non_blocking=True)          # every tensor's x (or the rotation's input)
@@ -709,7 +733,7 @@ def run_ours(args, world, rank, local):
 
     # read-only ceiling on the same box and buffers: one pn_read_ranges
     # launch per step reads the step's weight copies once (16-byte loads, no
-    # decode), in CUDA graphs like the GEMV steps
+    # decode), in CUDA graphs like the GEMV steps, after the same pre-heat
     sink = torch.zeros(len(tensors), dtype=torch.int32, device=dev)
 
     def read_step(i):
@@ -723,7 +747,14 @@ def run_ours(args, world, rank, local):
             for i in range(nodes):
                 read_step(i)
         gr.replay()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < PREHEAT_S:
+        with torch.cuda.stream(stream):
+            for _ in range(4):
+                gr.replay()
         torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
         r0 = torch.cuda.Event(enable_timing=True)
         r1 = torch.cuda.Event(enable_timing=True)
         r_reps = max(1, reps)
@@ -731,7 +762,7 @@ def run_ours(args, world, rank, local):
         for _ in range(r_reps):
             gr.replay()
         r1.record(stream)
-        torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
     r_us = r0.elapsed_time(r1) * 1e3 / (r_reps * nodes)
     read_ceiling = {"us_per_step": r_us, "gbs": wbytes / (r_us / 1e6) / 1e9,
                     "time_frac": r_us / (ms_per_step * 1e3),
@@ -741,40 +772,77 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak()
     per_gpu = step_bytes / (ms_per_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s",
-                "frac": per_gpu / peak, "traffic": recorded_traffic(args.config) if default_m else None,
+                "frac": per_gpu / peak,
+                "traffic": recorded_traffic(cfg) if (default_m and not args.hadamard and args.algo == "auto")
+                else None,
                 "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+    launches = args.steps * ((1 if len(tensors) == 1 or algo != pn.ALGO_CUDA_CORE else len(tensors))
+                             + (len(tensors) if args.hadamard else 0))
+    return {
+        "name": name, "tensors": tensors, "M": M, "value": value, "ms_per_step": ms_per_step,
+        "step_bytes": step_bytes, "wbytes": wbytes, "copies": copies, "nodes": nodes,
+        "per_gpu": per_gpu, "roofline": roofline, "read_ceiling": read_ceiling, "clocks": clock_info,
+        "e2e": e2e, "launches": launches, "preheat_ms": preheat_ms, "preheat_steps": preheat_steps,
+    }
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from bit_weight_only_pn_gb300 import build, pn
+    if rank == 0 or not os.path.exists(pn.LIBRARY):
+        build.build()             # no-op when the library is up to date
+    dist_barrier(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    r = measure_gemv(args, args.config, args.m, world, dev, args.e2e_steps)
+    # the metric's other half: the skinny verification batch (M = 8) over the
+    # 27B-class layer, timed the same way, in the same line
+    m8 = None
+    if not args.no_m8 and args.config != 4 and not args.m:
+        q = measure_gemv(args, 4, 0, world, dev, min(args.e2e_steps, 200))
+        m8 = {"workload": q["name"], "M": q["M"], "us_per_gemv": q["ms_per_step"] * 1e3,
+              "value": q["value"], "unit": "GB/s", "steps": args.steps, "warmup": args.warmup,
+              "pct_of_nominal_8tbs": q["per_gpu"] / NOMINAL_HBM_GBS * 100.0,
+              "algorithmic_bytes_per_step": q["step_bytes"],
+              "roofline": q["roofline"], "read_ceiling": q["read_ceiling"], "clocks": q["clocks"],
+              "e2e": q["e2e"], "gpu_launches": q["launches"], "preheat_ms": q["preheat_ms"]}
+        del q
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        rate, desc, used, _ = oracle_sample_rate(tensors, M, args.cpu_seconds, os.cpu_count() or 1)
-        rate1, desc1, _, _ = oracle_sample_rate(tensors, M, args.cpu_seconds / 2, 1)
+        rate, desc, used, _ = oracle_sample_rate(r["tensors"], r["M"], args.cpu_seconds, os.cpu_count() or 1)
+        rate1, desc1, _, _ = oracle_sample_rate(r["tensors"], r["M"], args.cpu_seconds / 2, 1)
         cpu = {"value": rate, "unit": "GB/s", "cores": used, "kind": "oracle", "sample": desc,
                "value_one_core": rate1, "sample_one_core": desc1, "cpu_model": cpu_model()}
 
     if rank != 0:
         return
+    tensors = r["tensors"]
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 products, f32 accumulate",
         "data": "synthetic",
-        "config": {"workload": name, "M": M,
+        "config": {"workload": r["name"], "M": r["M"],
                    "tensors": [f"{'pn3t' if t == 124 else 'pn4t'} {K}->{N}" for t, K, N in tensors],
-                   "algorithmic_bytes_per_step": step_bytes, "weight_bytes_per_step": wbytes,
-                   "l2": f"{copies} rotating weight copies ({copies * wbytes / 1e6:.0f} MB > 2x L2)",
-                   "launch": f"CUDA graph of {nodes} steps, replayed",
+                   "algorithmic_bytes_per_step": r["step_bytes"], "weight_bytes_per_step": r["wbytes"],
+                   "l2": f"{r['copies']} rotating weight copies ({r['copies'] * r['wbytes'] / 1e6:.0f} MB > 2x L2)",
+                   "launch": f"CUDA graph of {r['nodes']} steps, replayed; every graph replayed and "
+                             f"{PREHEAT_S:.1f} s of replays untimed before the timed region",
                    "parallelism": "replicas" if world > 1 else "1 GPU",
                    "algo": args.algo,
                    "hadamard_block": args.hadamard or None},
-        "us_per_gemv": ms_per_step * 1e3,
-        "pct_of_nominal_8tbs": per_gpu / NOMINAL_HBM_GBS * 100.0,
-        "gpu_launches": args.steps * ((1 if len(tensors) == 1 or algo != pn.ALGO_CUDA_CORE else len(tensors))
-                                      + (len(tensors) if args.hadamard else 0)),
-        "roofline": roofline,
-        "read_ceiling": read_ceiling,
-        "clocks": clock_info,
-        "e2e": e2e,
+        "us_per_gemv": r["ms_per_step"] * 1e3,
+        "pct_of_nominal_8tbs": r["per_gpu"] / NOMINAL_HBM_GBS * 100.0,
+        "gpu_launches": r["launches"],
+        "preheat_ms": r["preheat_ms"],
+        "roofline": r["roofline"],
+        "read_ceiling": r["read_ceiling"],
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+        "m8": m8,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -66,15 +66,28 @@ def test_kernel_source_hash_is_stable_and_per_kernel():
 
 def test_recorded_traffic_only_for_the_current_sources(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "pn_gemv_traffic.md").write_text(
-        "notes\n"
-        "traffic config=1 kernel=gemv_stream_kernel<8> bytes_per_launch=111 source=aaaa\n"
-        "traffic config=4 kernel=gemv_tc_kernel<1> bytes_per_launch=444 source=bbbb\n")
+    (tmp_path / "profiles" / "traffic.json").write_text(
+        '{"records": ['
+        '{"config": 1, "kernel": "gemv_stream_kernel<8>", "bytes_per_launch": 111, "source": "aaaa"},'
+        '{"config": 4, "kernel": "gemv_tc_kernel<1>", "bytes_per_launch": 444, "source": "bbbb"}]}')
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: {"stream": "aaaa", "tc": "cccc"}.get(k, "x"))
     assert bench.recorded_traffic(1) == 111          # taken on the current stream sources
     assert bench.recorded_traffic(4) is None         # the batch kernel changed since
     assert bench.recorded_traffic(2) is None         # never captured
+    (tmp_path / "profiles" / "traffic.json").write_text("not json")
+    assert bench.recorded_traffic(1) is None
+
+
+def test_committed_traffic_records_are_well_formed():
+    import json
+    with open(os.path.join(ROOT, bench.TRAFFIC_FILE)) as fh:
+        records = json.load(fh)["records"]
+    assert records
+    for r in records:
+        assert set(r) >= {"config", "kernel", "bytes_per_launch", "source"}
+        assert r["config"] in range(7)
+        assert int(r["bytes_per_launch"]) > 0 and len(r["source"]) == 16
 
 
 def test_measured_peak_reads_the_driver_file(tmp_path, monkeypatch):
