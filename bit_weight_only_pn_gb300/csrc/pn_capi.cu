@@ -95,22 +95,30 @@ bool tc_eligible(const pn::GemvTensor& t) {
     return t.nb % 8 == 0 && aligned(t.W, 16) && aligned(t.x, 16);
 }
 
+// Sorts the tensors of a call into the tensor-core and CUDA-core kernels.
+pn_status route(const pn::GemvTensor* ts, int count, int algo, int major, pn::GemvTensor* tc, int* ntc,
+                pn::GemvTensor* simt, int* nsimt) {
+    if (algo != PN_ALGO_AUTO && algo != PN_ALGO_TENSOR_CORE && algo != PN_ALGO_CUDA_CORE) return PN_EINVAL;
+    *ntc = *nsimt = 0;
+    for (int e = 0; e < count; ++e) {
+        if (ts[e].N == 0) continue;
+        const bool ok_tc = tc_eligible(ts[e]) && major >= 10;
+        if (algo == PN_ALGO_TENSOR_CORE && !ok_tc) return major >= 10 ? PN_EALIGN : PN_EUNSUPPORTED;
+        if (algo != PN_ALGO_CUDA_CORE && ok_tc) tc[(*ntc)++] = ts[e];
+        else simt[(*nsimt)++] = ts[e];
+    }
+    return PN_OK;
+}
+
 pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t ws_bytes, int algo,
                     cudaStream_t s) {
     int sms = 0, major = 0;
     pn_status st = device_info(&sms, &major);
     if (st != PN_OK) return st;
-    if (algo != PN_ALGO_AUTO && algo != PN_ALGO_TENSOR_CORE && algo != PN_ALGO_CUDA_CORE) return PN_EINVAL;
     pn::GemvTensor tc[pn::kMaxLayer];
     pn::GemvTensor simt[pn::kMaxLayer];
     int ntc = 0, nsimt = 0;
-    for (int e = 0; e < count; ++e) {
-        if (ts[e].N == 0) continue;
-        const bool ok_tc = tc_eligible(ts[e]) && major >= 10;
-        if (algo == PN_ALGO_TENSOR_CORE && !ok_tc) return major >= 10 ? PN_EALIGN : PN_EUNSUPPORTED;
-        if (algo != PN_ALGO_CUDA_CORE && ok_tc) tc[ntc++] = ts[e];
-        else simt[nsimt++] = ts[e];
-    }
+    if ((st = route(ts, count, algo, major, tc, &ntc, simt, &nsimt)) != PN_OK) return st;
     if (ntc > 0) {
         if (!ws || !aligned(ws, 256)) return PN_EINVAL;
         const pn::WorkspaceLayout L = pn::workspace_layout(sms);
@@ -224,6 +232,27 @@ pn_status pn_workspace_status(void* workspace, size_t workspace_bytes, pn_stream
     if (cudaError_t e2 = cudaMemset(workspace, 0, workspace_bytes); e2 != cudaSuccess) return pn::cuda_error(e2);
     return word == PN_ETIMEOUT ? PN_ETIMEOUT : PN_ECUDA;
 }
+
+}  // extern "C"
+
+namespace pn {
+pn_status gemv_check(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M, float* y,
+                     int algo, bool* uses_workspace) {
+    *uses_workspace = false;
+    pn::GemvTensor t{};
+    pn_status st = check_tensor(type, W, N, K, x, M, y, &t);
+    if (st != PN_OK || N == 0) return st;
+    int sms = 0, major = 0;
+    if ((st = device_info(&sms, &major)) != PN_OK) return st;
+    pn::GemvTensor tc[1], simt[1];
+    int ntc = 0, nsimt = 0;
+    if ((st = route(&t, 1, algo, major, tc, &ntc, simt, &nsimt)) != PN_OK) return st;
+    *uses_workspace = ntc > 0;
+    return PN_OK;
+}
+}  // namespace pn
+
+extern "C" {
 
 pn_status pn_gemv_ex(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M,
                      float* y, void* workspace, size_t workspace_bytes, int algo, pn_stream stream) {

@@ -158,4 +158,11 @@ int tc_max_ctas(int num_sms);
 bool tc_split(const GemvTensor* t, int count, int M, int num_sms, int* grid, uint32_t* starts);
 size_t tc_partial_bytes(int num_sms);
 
+// Host-side checks of a one-tensor GEMV, the same ones pn_gemv_ex makes before
+// it launches anything.  On PN_OK, *uses_workspace tells whether the call
+// would launch a tensor-core kernel (which reads and writes the workspace; the
+// CUDA-core kernel does not, nor does a call with N = 0).
+pn_status gemv_check(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M, float* y,
+                     int algo, bool* uses_workspace);
+
 }  // namespace pn

@@ -57,25 +57,28 @@ pn_status scratch_address(void** out) {
 
 extern "C" pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const uint16_t* x,
                                      int M, float* y, pn_stream stream) {
+    // Every argument check first, so a refused call enqueues nothing.
+    bool uses_ws = false;
+    pn_status st = pn::gemv_check(type, W, N, K, x, M, y, PN_ALGO_AUTO, &uses_ws);
+    if (st != PN_OK) return st;
+    if (N == 0) return PN_OK;
     // The workspace this call needs on the current device; beyond the fixed
     // array (a device with more SMs than it was sized for) the call is refused.
-    const size_t need = pn_workspace_bytes(N > 0 ? N : 1);
-    if (need == 0) return PN_ECUDA;
-    if (need > kNoAllocScratchBytes) return PN_EINVAL;
-    void* ws = nullptr;
-    pn_status st = scratch_address(&ws);
-    if (st != PN_OK) return st;
-    // The array keeps the last call's contents.  The status word, the tagged
-    // hand-off words and the counters must start at zero; a completed call
-    // leaves them zero, an aborted one may not, so the whole workspace is
-    // cleared before every launch.
     int sms = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return pn::cuda_error(e);
     const pn::WorkspaceLayout L = pn::workspace_layout(sms);
-    if ((e = cudaMemsetAsync(ws, 0, L.total, reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+    if (L.total > kNoAllocScratchBytes) return PN_EINVAL;
+    void* ws = nullptr;
+    if ((st = scratch_address(&ws)) != PN_OK) return st;
+    // The array keeps the last call's contents.  The status word, the tagged
+    // hand-off words and the counters must start at zero; a completed call
+    // leaves them zero, an aborted one may not, so the workspace is cleared on
+    // the stream before every call that launches a kernel using it (the
+    // CUDA-core kernel does not).
+    if (uses_ws && (e = cudaMemsetAsync(ws, 0, L.total, reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
         return pn::cuda_error(e);
     return pn_gemv_ex(type, W, N, K, x, M, y, ws, kNoAllocScratchBytes, PN_ALGO_AUTO, stream);
 }

@@ -190,8 +190,12 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
  * PN_EINVAL and nothing is launched.  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress, which may load the
  * library's device module); make that first call before capturing a stream
- * into a CUDA graph.  Every call shares the array and it keeps the last call's
- * contents: each call first clears, on `stream`, the parts that must start at
+ * into a CUDA graph.  The address is kept for the life of the process: after
+ * cudaDeviceReset on a device, do not call pn_gemv_noalloc on that device
+ * again (the array may have moved).  Arguments are checked first, exactly as
+ * pn_gemv checks them; a refused call enqueues nothing.  Every call shares the
+ * array and it keeps the last call's contents: each call that launches a
+ * tensor-core kernel first clears, on `stream`, the parts that must start at
  * zero.  Calls whose executions overlap on the GPU (other streams, other host
  * threads) race on the array and give wrong results; order them on one
  * stream.  A device-side wait that gives up (see pn_set_wait_timeout_ns)
