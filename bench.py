@@ -565,6 +565,7 @@ def run_reference_prefill(args, world, rank):
 
 
 PREHEAT_S = 0.5              # untimed graph replays before every timed region
+SLEEP_CYCLES = 400_000       # about 0.2 ms of GPU sleep ahead of each timed region
 
 
 def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
@@ -677,6 +678,10 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
     dist_barrier(world)
     torch.cuda.synchronize(dev)
     clocks.mark()
+    # the GPU waits on a short sleep kernel while the host enqueues the start
+    # event and the graphs, so no host launch latency falls inside the region
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(SLEEP_CYCLES)
     start.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(reps):
@@ -758,6 +763,7 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
         r0 = torch.cuda.Event(enable_timing=True)
         r1 = torch.cuda.Event(enable_timing=True)
         r_reps = max(1, reps)
+        torch.cuda._sleep(SLEEP_CYCLES)
         r0.record(stream)
         for _ in range(r_reps):
             gr.replay()

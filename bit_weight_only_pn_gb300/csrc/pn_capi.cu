@@ -125,8 +125,8 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
         if (L.total > ws_bytes) return PN_EINVAL;
         uint8_t* base = static_cast<uint8_t*>(ws);
         uint32_t* status = reinterpret_cast<uint32_t*>(base + L.status);
-        // one or two tokens: every warp streams its own units; more: thread
-        // blocks share each staged activation chunk among eight tiles
+        // one or two tokens: one block per SM streams a range of units; more:
+        // thread blocks share each staged activation chunk among eight tiles
         cudaError_t e = M <= 2
             ? pn::launch_gemv_stream(tc, ntc, M, status, reinterpret_cast<uint64_t*>(base + L.tagged), sms,
                                      g_timeout_ns.load(), g_test_stall.load(), s)

@@ -91,6 +91,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// One probe of phase `parity` that may suspend the thread until the phase
+// completes or about `hint_ns` nanoseconds pass (mbarrier.try_wait with a
+// suspend-time hint); true once the phase has completed.  A suspended warp
+// issues nothing, so waiting warps leave the issue slots to working ones.
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+    return done != 0;
+}
+
 // Bulk copy (TMA engine, no tensor map) of `bytes` (multiple of 16, both
 // addresses 16-byte aligned) from global to this CTA's shared memory; the
 // byte count is credited to the transaction count of `bar`.

@@ -141,7 +141,8 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int num_sms);
 
 // Tensor-core GEMV for M <= 2 over `count` tensors (every one with nb % 8 == 0
-// and W, x 16-byte aligned): every warp streams its own units.
+// and W, x 16-byte aligned): one block per SM streams a contiguous range of
+// units through a TMA ring that its warps share.
 cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* status, uint64_t* tagged,
                                int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s);
 int stream_max_ctas(int num_sms);
