@@ -125,9 +125,12 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
         if (L.total > ws_bytes) return PN_EINVAL;
         uint8_t* base = static_cast<uint8_t*>(ws);
         uint32_t* status = reinterpret_cast<uint32_t*>(base + L.status);
-        // one or two tokens: one block per SM streams a range of units; more:
+        // one or two tokens: one block per SM streams a range of units (rows of
+        // at most stream_max_chunks() chunks); more tokens or longer rows:
         // thread blocks share each staged activation chunk among eight tiles
-        cudaError_t e = M <= 2
+        bool stream = M <= 2;
+        for (int i = 0; i < ntc; ++i) stream = stream && tc[i].nb / 8 <= pn::stream_max_chunks();
+        cudaError_t e = stream
             ? pn::launch_gemv_stream(tc, ntc, M, status, reinterpret_cast<uint64_t*>(base + L.tagged), sms,
                                      g_timeout_ns.load(), g_test_stall.load(), s)
             : pn::launch_gemv_tc(tc, ntc, M, status, reinterpret_cast<float*>(base + L.partials),

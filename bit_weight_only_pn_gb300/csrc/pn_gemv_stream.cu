@@ -75,7 +75,7 @@ constexpr int kStages = 1 << kStagesLog2;                 // ring stages (a powe
 constexpr int kPartsLog2 = 6;
 constexpr int kParts = 1 << kPartsLog2;                   // partial-sum slots in shared memory
 constexpr int kSlotFloats = kRows * kStreamMaxM;          // [row][token]
-constexpr int kZeroBytes = 256;                           // zeros read by lanes with an empty B fragment
+constexpr int kZeroBytes = 512;                           // zeros read by lanes with an empty B fragment
 constexpr int kMaxGrid = 512;                             // thread blocks per launch, at most
 constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                    // PN_ETIMEOUT
@@ -90,7 +90,8 @@ __host__ __device__ constexpr int stage_bytes(int M) { return (kBoxBytes + M * k
 // empty barriers, the partial-sum slots with their generation words and tile
 // counters, the ticket counter, the abort flag and zeros.
 struct SmemLayout {
-    int sbytes = 0, table = 0, full = 0, empty = 0, parts = 0, gens = 0, cnts = 0, misc = 0, zeros = 0, total = 0;
+    int sbytes = 0, table = 0, full = 0, empty = 0, parts = 0, gens = 0, cnts = 0, xown = 0, misc = 0, zeros = 0,
+        total = 0;
     __host__ __device__ constexpr explicit SmemLayout(int M) {
         sbytes = stage_bytes(M);
         table = kStages * sbytes;
@@ -99,7 +100,8 @@ struct SmemLayout {
         parts = empty + 8 * kStages;
         gens = parts + kParts * kSlotFloats * 4;
         cnts = gens + 4 * kParts;
-        misc = cnts + 4 * kParts;             // ticket (4), abort (4)
+        xown = cnts + 4 * kParts;             // one-token units: each consumer's copy of the activations
+        misc = xown + (M == 1 ? kConsumers * kXTokenBytes : 0);   // ticket (4), abort (4)
         zeros = (misc + 8 + 15) / 16 * 16;
         total = zeros + kZeroBytes;
     }
@@ -198,6 +200,8 @@ __device__ __forceinline__ void load_pairs(const uint8_t* p, uint32_t (&v)[NP]) 
     }
 }
 
+__device__ __forceinline__ int lane_id() { return static_cast<int>(threadIdx.x & 31); }
+
 __device__ __forceinline__ float lds_half(const uint8_t* p) { return __half2float(*reinterpret_cast<const __half*>(p)); }
 
 // Per-unit context of a lane.
@@ -206,6 +210,7 @@ struct Lane {
     const uint8_t* r0;     // staged row g
     const uint8_t* r1;     // staged row g + 8
     const uint8_t* x;      // staged activations of token 0 (token m at + m * kXTokenBytes)
+    uint8_t* xown;         // this warp's own copy of one token's activations (one-token units)
     const uint8_t* zeros;  // kZeroBytes of zeros
 };
 
@@ -214,8 +219,8 @@ struct Lane {
 // sums to acc: acc[h] = row g + 8h of token tok(t).
 // ---------------------------------------------------------------------------
 
-template <int TYPE>
-__device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4]) {
+template <int TYPE, typename Release>
+__device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4], Release&& release) {
     using F = Format<TYPE>;
     constexpr int kP = F::kPairs;
     const int g = L.g, t = L.t;
@@ -225,30 +230,54 @@ __device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4]) {
     // B columns are the blocks: lane g == 2t+1 carries block 2t+1's
     // activations in b0, lane g == 2t block 2t's in b1, every other B
     // register is zero.
-    const uint8_t* xo = (g == 2 * t + 1) ? L.x + (2 * t + 1) * F::kPerBlock * 2 : L.zeros;
-    const uint8_t* xe = (g == 2 * t) ? L.x + 2 * t * F::kPerBlock * 2 : L.zeros;
     // block 2t starts 4-byte aligned in a staged row: aligned word i at byte
     // 4i holds (previous half, next half), so code word i is one byte permute
     // of aligned words i and i+1; word 0 also holds the even block's scale,
-    // word 8 the odd block's.  The code words are loaded word by word, next to
-    // the MMAs that use them, which keeps few of them live at once.
+    // word 8 the odd block's.  The unit's code words (rows g and g+8 of blocks
+    // 2t and 2t+1) go to registers and its activations to this warp's own
+    // copy in shared memory first; then the stage is released, so the
+    // producer can refill it while the MMAs run.
     const uint8_t* e0 = L.r0 + 68 * t;
     const uint8_t* e1 = L.r1 + 68 * t;
-    uint32_t p0 = lds_u32(e0), p1 = lds_u32(e1);
-    const float d_e0 = half_lo(p0), d_e1 = half_lo(p1);
+    uint32_t we0[8], we1[8], wo0[8], wo1[8];
+    float d_e0, d_e1, d_o0, d_o1;
+    {
+        uint32_t a0[9], a1[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+            a0[i] = lds_u32(e0 + 4 * i);
+            a1[i] = lds_u32(e1 + 4 * i);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            we0[i] = prmt(a0[i], a0[i + 1], 0x5432u);
+            we1[i] = prmt(a1[i], a1[i + 1], 0x5432u);
+            wo0[i] = lds_u32(e0 + 36 + 4 * i);
+            wo1[i] = lds_u32(e1 + 36 + 4 * i);
+        }
+        d_e0 = half_lo(a0[0]);
+        d_e1 = half_lo(a1[0]);
+        d_o0 = half_hi(a0[8]);
+        d_o1 = half_hi(a1[8]);
+        // the chunk's activations (kXTokenBytes at most) to the private copy
+        constexpr int kVec = kChunkBlocks * F::kPerBlock * 2 / 16;
+#pragma unroll
+        for (int i = 0; i < (kVec + 31) / 32; ++i) {
+            const int j = lane_id() + 32 * i;
+            if (j < kVec) *reinterpret_cast<uint4*>(L.xown + 16 * j) = lds_u128(L.x + 16 * j);
+        }
+    }
+    release();                                          // (orders this warp's copy before its reads too)
+    const uint8_t* xo = (g == 2 * t + 1) ? L.xown + (2 * t + 1) * F::kPerBlock * 2 : L.zeros;
+    const uint8_t* xe = (g == 2 * t) ? L.xown + 2 * t * F::kPerBlock * 2 : L.zeros;
     float c[2][4];
 #pragma unroll
     for (int k = 0; k < 2; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = 0.0f;
     uint32_t bo[4], be[4];
     static_for<8>([&](auto wc) {
         constexpr int W = decltype(wc)::value;
-        const uint32_t n0 = lds_u32(e0 + 4 * (W + 1)), n1 = lds_u32(e1 + 4 * (W + 1));
-        const uint32_t we0 = prmt(p0, n0, 0x5432u), we1 = prmt(p1, n1, 0x5432u);
-        p0 = n0;
-        p1 = n1;
-        const uint32_t wo0 = lds_u32(e0 + 36 + 4 * W), wo1 = lds_u32(e1 + 36 + 4 * W);
-        const uint32_t so0 = wo0 >> F::kHighShift, so1 = wo1 >> F::kHighShift;
-        const uint32_t se0 = we0 >> F::kHighShift, se1 = we1 >> F::kHighShift;
+        const uint32_t so0 = wo0[W] >> F::kHighShift, so1 = wo1[W] >> F::kHighShift;
+        const uint32_t se0 = we0[W] >> F::kHighShift, se1 = we1[W] >> F::kHighShift;
         static_for<kP>([&](auto pc) {
             constexpr int Pp = decltype(pc)::value;
             constexpr int S = W * kP + Pp;
@@ -257,11 +286,10 @@ __device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4]) {
                 load_pairs<4>(xe + 4 * S, be);
             }
             mma_acc(c[S & 1],
-                    decode_pair<TYPE, Pp>(wo0, so0), decode_pair<TYPE, Pp>(wo1, so1),
-                    decode_pair<TYPE, Pp>(we0, se0), decode_pair<TYPE, Pp>(we1, se1), bo[S % 4], be[S % 4]);
+                    decode_pair<TYPE, Pp>(wo0[W], so0), decode_pair<TYPE, Pp>(wo1[W], so1),
+                    decode_pair<TYPE, Pp>(we0[W], se0), decode_pair<TYPE, Pp>(we1[W], se1), bo[S % 4], be[S % 4]);
         });
     });
-    const float d_o0 = half_hi(p0), d_o1 = half_hi(p1);        // aligned word 8: the odd block's scale
     // column 2t <-> block 2t (even), 2t+1 <-> block 2t+1 (odd)
     float r0 = d_e0 * (c[0][0] + c[1][0]);
     r0 = fmaf(d_o0, c[0][1] + c[1][1], r0);
@@ -275,8 +303,8 @@ __device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4]) {
     acc[1] += r1;
 }
 
-template <int TYPE>
-__device__ __forceinline__ void unit_b4(const Lane& L, int M, float (&acc)[4]) {
+template <int TYPE, typename Release>
+__device__ __forceinline__ void unit_b4(const Lane& L, int M, float (&acc)[4], Release&& release) {
     using F = Format<TYPE>;
     constexpr int kP = F::kPairs;
     const int g = L.g, t = L.t;
@@ -332,15 +360,15 @@ __device__ __forceinline__ void unit_b4(const Lane& L, int M, float (&acc)[4]) {
             acc[h] += v[h];
         }
     });
+    release();
 }
 
-template <int BPM, int TYPE>
-__device__ __forceinline__ void unit(const Lane& L, int M, float (&acc)[4]) {
-    if constexpr (BPM == 8) unit_b8<TYPE>(L, M, acc);
-    else unit_b4<TYPE>(L, M, acc);
+// One unit; release() is called once the unit no longer reads its stage.
+template <int BPM, int TYPE, typename Release>
+__device__ __forceinline__ void unit(const Lane& L, int M, float (&acc)[4], Release&& release) {
+    if constexpr (BPM == 8) unit_b8<TYPE>(L, M, acc, release);
+    else unit_b4<TYPE>(L, M, acc, release);
 }
-
-
 
 // ------------------------------------------------------------ tile results --
 
@@ -534,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     L.g = lane >> 2;
     L.t = lane & 3;
     L.zeros = smem + Lay.zeros;
+    L.xown = smem + Lay.xown + warp * kXTokenBytes;
     for (;;) {
         uint32_t k = 0;
         if (lane == 0) k = atomicAdd(ticket, 1u);
@@ -567,19 +596,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         L.r1 = stage + (L.g + 8) * kChunkBytes;
         L.x = stage + kBoxBytes;
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (((rec.chunk_e_flags >> 30) & 1u) == 0u) unit<BPM, kPn3t>(L, P.M, acc);
-        else unit<BPM, kPn4t>(L, P.M, acc);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);      // the stage may be refilled
+        auto release = [&] {                              // the stage may be refilled
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        };
+        if (((rec.chunk_e_flags >> 30) & 1u) == 0u) unit<BPM, kPn3t>(L, P.M, acc, release);
+        else unit<BPM, kPn4t>(L, P.M, acc, release);
         // the unit's partials to slot k of the ring, once its previous user
         // (ticket k - kParts, a lower ticket) has been combined; the tile's
         // counter is in the slot of the tile's first ticket
         const uint32_t slot = k & (kParts - 1), fslot = rec.k_first & (kParts - 1);
         bool ok = true;
-        if (lane == 0)
-            ok = smem_wait_eq(gens + slot, k >> kPartsLog2, P.timeout_ns, abort_flag) &&
-                 smem_wait_eq(gens + fslot, rec.k_first >> kPartsLog2, P.timeout_ns, abort_flag);
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+        // (every lane reads the same words, so the branch is uniform)
+        if (gens[slot] != (k >> kPartsLog2) || gens[fslot] != (rec.k_first >> kPartsLog2)) {
+            if (lane == 0)
+                ok = smem_wait_eq(gens + slot, k >> kPartsLog2, P.timeout_ns, abort_flag) &&
+                     smem_wait_eq(gens + fslot, rec.k_first >> kPartsLog2, P.timeout_ns, abort_flag);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        }
+        if (!ok) {
             if (lane == 0) {
                 *abort_flag = 1u;
                 atomicCAS(P.status, 0u, kStatusTimeout);
@@ -677,6 +712,8 @@ static_assert(SmemLayout(kStreamMaxM).total <= 227 * 1024, "the two-token layout
 
 }  // namespace
 
+int stream_max_chunks() { return kParts; }
+
 int stream_max_ctas(int num_sms) { return num_sms < kMaxGrid ? num_sms : kMaxGrid; }
 
 size_t stream_tagged_bytes(int num_sms) {
@@ -700,8 +737,8 @@ cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* 
         T.tiles = (t[e].N + kRows - 1) / kRows;
         T.unit_base = static_cast<uint32_t>(units);
         if (!encode_rows(&P.wmap[e], t[e])) return cudaErrorInvalidValue;
-        // chunk numbers travel in 24 bits of a stage record
-        if (T.chunks >= (1 << 24)) return cudaErrorInvalidValue;
+        // a tile's chunk partials must all fit the shared-memory slot ring
+        if (T.chunks > kParts) return cudaErrorInvalidValue;
         units += static_cast<uint64_t>(T.chunks) * T.tiles;
         max_chunks = T.chunks > max_chunks ? T.chunks : max_chunks;
     }

@@ -147,6 +147,8 @@ cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* 
                                int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s);
 int stream_max_ctas(int num_sms);
 size_t stream_tagged_bytes(int num_sms);
+// Longest row (in 8-block chunks) the one-/two-token kernel takes.
+int stream_max_chunks();
 
 // Tensor-core GEMV for 3 <= M <= 16 (same eligibility): thread blocks share
 // each staged activation chunk among eight tiles.

@@ -287,3 +287,28 @@ def test_layer_small_full_compare(pn, dev, oracle):
             assert ws.status() == 0
             for (t, Wd, K, xd, y), (y_ref, abs_sum) in zip(entries, refs):
                 assert_gemv_close(y.cpu().numpy(), y_ref, abs_sum)
+
+
+@pytest.mark.parametrize("pn_type", TYPES)
+def test_gemv_long_rows_one_and_two_tokens(pn, dev, oracle, pn_type):
+    # rows longer than the one-token kernel takes (more than 64 chunks of 8
+    # blocks) go to the batch kernel at M = 1 and 2 as well; every output
+    # against the oracle, single tensors and a mixed layer call
+    bpb = GEOMETRY[pn_type][0]
+    N, K = 300, 65 * 8 * bpb
+    W, x = synth_case(oracle, pn_type, N, K, 2, 0x65)
+    Wd = to_dev(W, dev)
+    ws = pn.Workspace(N + 200, dev)
+    for M in (1, 2):
+        y_ref, abs_sum = oracle.gemv(pn_type, W, K, x[:M])
+        y = pn.gemv(pn_type, Wd, K, to_dev(x[:M], dev), workspace=ws).cpu().numpy()
+        assert ws.status() == 0
+        assert_gemv_close(y, y_ref, abs_sum)
+        W2, x2 = synth_case(oracle, PN3T, 200, 640, M, 0x66)
+        entries = [(pn_type, Wd, K, to_dev(x[:M], dev), torch.empty((M, N), dtype=torch.float32, device=dev)),
+                   (PN3T, to_dev(W2, dev), 640, to_dev(x2, dev), torch.empty((M, 200), dtype=torch.float32, device=dev))]
+        pn.gemv_layer(entries, M, workspace=ws)
+        assert ws.status() == 0
+        assert_gemv_close(entries[0][4].cpu().numpy(), y_ref, abs_sum)
+        y2_ref, a2 = oracle.gemv(PN3T, W2, 640, x2)
+        assert_gemv_close(entries[1][4].cpu().numpy(), y2_ref, a2)
