@@ -77,6 +77,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_unpack_f16.argtypes = [ctypes.c_int, c_void_p, i64, i64, c_void_p]
     lib.oracle_gemm_f16.restype = ctypes.c_int
     lib.oracle_gemm_f16.argtypes = [c_void_p, i64, i64, c_void_p, ctypes.c_int, c_void_p, c_void_p]
+    if hasattr(lib, "oracle_gptq"):
+        lib.oracle_gptq.restype = ctypes.c_int
+        lib.oracle_gptq.argtypes = [ctypes.c_int, c_void_p, i64, i64, c_void_p, i64, ctypes.c_double, c_void_p]
     return lib
 
 
@@ -210,6 +213,21 @@ class Oracle:
         if rc:
             raise ValueError(f"oracle_gemm_f16 failed ({rc})")
         return (y, a) if want_abs else y
+
+    def gptq(self, pn_type: int, w: np.ndarray, X: np.ndarray, damp: float = 0.01) -> np.ndarray:
+        """GPTQ-style quantisation (reading R12) of fp32 weights [N][K] with
+        calibration inputs X [n][K]: PN bytes [N][row_bytes]."""
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        X = np.ascontiguousarray(X, dtype=np.float32)
+        N, K = w.shape
+        if X.ndim != 2 or X.shape[1] != K:
+            raise ValueError("calibration inputs must be [n][K]")
+        out = np.zeros((N, self.row_bytes(pn_type, K)), dtype=np.uint8)
+        rc = self.lib.oracle_gptq(pn_type, w.ctypes.data, N, K, X.ctypes.data, X.shape[0], float(damp),
+                                  out.ctypes.data)
+        if rc:
+            raise ValueError(f"oracle_gptq failed ({rc})")
+        return out
 
     def half_to_float(self, h: int) -> float:
         return float(self.lib.oracle_half_to_float(h))

@@ -31,6 +31,17 @@
  *       saturated to +-65504.  Inputs must be finite.
  *   R5  GEMV y[m][r] = sum_k w[r][k] * x[m][k]: products and the sum in fp64,
  *       sequential in k, rounded to fp32 once.
+ *   R12 GPTQ-style quantiser (tensorless docs, "How Qwen3.8-27B-PN3 uses it",
+ *       says only "GPTQ-style"): the published GPTQ procedure (Frantar et al.,
+ *       "GPTQ: Accurate Post-Training Quantization for Generative
+ *       Pre-trained Transformers", ICLR 2023, Algorithm 1) with PN blocks as
+ *       its groups.  H = 2 X^T X + lambda I over calibration inputs X [n][K],
+ *       lambda = damp * mean(diag(2 X^T X)); U = the upper Cholesky factor of
+ *       H^-1 (H^-1 = U^T U).  Columns k = 0 .. K-1 in order; when k starts a
+ *       block, each row's scale comes from the block's current weights
+ *       (rounded to fp32) by rule R4; column k is quantised by R4 with that
+ *       scale, and the error (w - decoded) / U[k][k] is subtracted, times
+ *       U[k][j], from every later column j.  All of it in fp64.
  *
  * Build: cc -O2 -std=c11 -fno-fast-math -ffp-contract=off -shared -fPIC.
  * -ffp-contract=off keeps every multiply and add a separately rounded IEEE
@@ -38,6 +49,7 @@
  * each with one planted mistake, to show that the pins catch such mistakes.)
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <string.h>
@@ -376,4 +388,141 @@ int oracle_gemm_f16(const uint16_t* w16, int64_t N, int64_t K, const uint16_t* x
         }
     }
     return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------- GPTQ ---- */
+
+/* Cholesky factor of the symmetric positive definite n x n matrix a (fp64,
+ * row-major): a = c c^T with c lower triangular, written over c.  Returns 0 if
+ * a pivot is not positive. */
+static int cholesky_lower(const double* a, double* c, int64_t n)
+{
+    for (int64_t i = 0; i < n * n; ++i) c[i] = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double s = a[j * n + j];
+        for (int64_t k = 0; k < j; ++k) s -= c[j * n + k] * c[j * n + k];
+        if (!(s > 0.0)) return 0;
+        double cjj = sqrt(s);
+        c[j * n + j] = cjj;
+        for (int64_t i = j + 1; i < n; ++i) {
+            double t = a[i * n + j];
+            for (int64_t k = 0; k < j; ++k) t -= c[i * n + k] * c[j * n + k];
+            c[i * n + j] = t / cjj;
+        }
+    }
+    return 1;
+}
+
+/* Inverse of the symmetric positive definite matrix a from its Cholesky
+ * factor c (a = c c^T): a^-1 = c^-T c^-1, column by column by forward and back
+ * substitution. */
+static void spd_inverse(const double* c, double* inv, double* tmp, int64_t n)
+{
+    for (int64_t col = 0; col < n; ++col) {
+        for (int64_t i = 0; i < n; ++i) {            /* c y = e_col */
+            double s = (i == col) ? 1.0 : 0.0;
+            for (int64_t k = 0; k < i; ++k) s -= c[i * n + k] * tmp[k];
+            tmp[i] = s / c[i * n + i];
+        }
+        for (int64_t i = n - 1; i >= 0; --i) {       /* c^T x = y */
+            double s = tmp[i];
+            for (int64_t k = i + 1; k < n; ++k) s -= c[k * n + i] * inv[k * n + col];
+            inv[i * n + col] = s / c[i * n + i];
+        }
+    }
+}
+
+/* Scale bits of one block from its current weights (rule R4), and whether it
+ * is the zero block. */
+static uint16_t block_scale(const oracle_fmt* f, const float* v, int* zero_block)
+{
+    int jmax = 0;
+    float amax = fabsf(v[0]);
+    for (int j = 1; j < f->per_block; ++j)
+        if (fabsf(v[j]) > amax) { amax = fabsf(v[j]); jmax = j; }
+    float a = v[jmax];
+    *zero_block = (a == 0.0f);
+    if (*zero_block) return 0;
+    uint16_t dbits = oracle_float_to_half(a / (float)(-f->zero));
+    if ((dbits & 0x7FFFu) == 0) { *zero_block = 1; return 0; }
+    if ((dbits & 0x7FFFu) == 0x7C00u) dbits = (uint16_t)((dbits & 0x8000u) | 0x7BFFu);
+    return dbits;
+}
+
+/* GPTQ-style quantisation (reading R12) of fp32 weights w[N][K] with
+ * calibration inputs X[n][K] (fp32) and dampening `damp` (> 0) into PN rows
+ * out[N][row_bytes]. */
+int oracle_gptq(int type, const float* w, int64_t N, int64_t K, const float* X, int64_t n, double damp,
+                uint8_t* out)
+{
+    oracle_fmt f;
+    if (!oracle_format(type, &f) || N < 0 || K <= 0 || K % f.per_block || !w || !out || !X || n < 1 ||
+        !(damp > 0.0))
+        return ORACLE_EINVAL;
+    const int64_t nb = K / f.per_block, z = f.zero;
+    double* H = (double*)malloc(sizeof(double) * K * K);
+    double* C = (double*)malloc(sizeof(double) * K * K);
+    double* Hi = (double*)malloc(sizeof(double) * K * K);
+    double* tmp = (double*)malloc(sizeof(double) * K);
+    double* W = (double*)malloc(sizeof(double) * N * K);
+    float* cur = (float*)malloc(sizeof(float) * f.per_block);
+    uint16_t* dbits = (uint16_t*)malloc(sizeof(uint16_t) * (N > 0 ? N : 1));
+    int* zero_blk = (int*)malloc(sizeof(int) * (N > 0 ? N : 1));
+    int* codes = (int*)malloc(sizeof(int) * (N * K > 0 ? N * K : 1));
+    int rc = ORACLE_OK;
+    if (!H || !C || !Hi || !tmp || !W || !cur || !dbits || !zero_blk || !codes) { rc = ORACLE_EINVAL; goto done; }
+    /* H = 2 X^T X, then dampened */
+    for (int64_t i = 0; i < K; ++i)
+        for (int64_t j = 0; j < K; ++j) {
+            double s = 0.0;
+            for (int64_t t = 0; t < n; ++t) s += (double)X[t * K + i] * (double)X[t * K + j];
+            H[i * K + j] = 2.0 * s;
+        }
+    double mean_diag = 0.0;
+    for (int64_t i = 0; i < K; ++i) mean_diag += H[i * K + i];
+    mean_diag /= (double)K;
+    for (int64_t i = 0; i < K; ++i) H[i * K + i] += damp * mean_diag;
+    /* U: upper Cholesky factor of H^-1 (H^-1 = U^T U, U = the transpose of
+     * the lower factor of H^-1) */
+    if (!cholesky_lower(H, C, K)) { rc = ORACLE_EINVAL; goto done; }
+    spd_inverse(C, Hi, tmp, K);
+    if (!cholesky_lower(Hi, C, K)) { rc = ORACLE_EINVAL; goto done; }   /* C lower; U[k][j] = C[j][k] */
+    for (int64_t i = 0; i < N * K; ++i) W[i] = (double)w[i];
+    for (int64_t k = 0; k < K; ++k) {
+        const int64_t b = k / f.per_block, kk = k % f.per_block;
+        if (kk == 0)
+            for (int64_t r = 0; r < N; ++r) {
+                for (int j = 0; j < f.per_block; ++j) cur[j] = (float)W[r * K + b * f.per_block + j];
+                dbits[r] = block_scale(&f, cur, &zero_blk[r]);
+            }
+        const double ukk = C[k * K + k];
+        for (int64_t r = 0; r < N; ++r) {
+            int code = (int)z;
+            float wq = 0.0f;
+            if (!zero_blk[r]) {
+                float d = oracle_half_to_float(dbits[r]);
+                float q = rintf((float)W[r * K + k] / d);
+                if (q < (float)(-z)) q = (float)(-z);
+                if (q > (float)(z - 1)) q = (float)(z - 1);
+                code = (int)q + (int)z;
+                wq = d * q;
+            }
+            codes[r * K + k] = code;
+            const double err = (W[r * K + k] - (double)wq) / ukk;
+            for (int64_t j = k + 1; j < K; ++j) W[r * K + j] -= err * C[j * K + k];
+        }
+        if (kk == f.per_block - 1)                     /* the block is complete: write it */
+            for (int64_t r = 0; r < N; ++r) {
+                uint8_t* blk = out + (r * nb + b) * ORACLE_BLOCK_BYTES;
+                uint32_t words[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                for (int j = 0; j < f.per_block; ++j)
+                    words[code_word(&f, j)] |= (uint32_t)codes[r * K + b * f.per_block + j] << code_shift(&f, j);
+                blk[0] = (uint8_t)(dbits[r] & 0xFF);
+                blk[1] = (uint8_t)(dbits[r] >> 8);
+                for (int j = 0; j < 8; ++j) store_u32_le(blk + 2 + 4 * j, words[j]);
+            }
+    }
+done:
+    free(H); free(C); free(Hi); free(tmp); free(W); free(cur); free(dbits); free(zero_blk); free(codes);
+    return rc;
 }

@@ -455,12 +455,87 @@ def pin_gemm_f16_matches_gemv_on_grid(o):
         assert np.array_equal(o.gemm_f16(w16, e, want_abs=False)[0], w[:, k])
 
 
+# ---------------------------------------------------------------- GPTQ ----
+# Reading R12: the published GPTQ procedure (Frantar et al., ICLR 2023,
+# Algorithm 1) with PN blocks as its groups.  Its pins: a Hessian without
+# off-diagonal terms leaves nothing to feed forward, so the result is the
+# pinned round-to-nearest packer's; an independent fp64 restatement in the
+# optimal-brain-quantiser form (explicit inverse, downdated after every
+# column) gives the same codes and scales; and on correlated inputs the
+# feedback lowers the output error below round-to-nearest's.
+
+def _gptq_reference(pn_type, w, X, damp):
+    """Decoded weights [N][K] of GPTQ in the explicit-inverse form (numpy fp64)."""
+    bpb, _, _, z = GEOMETRY[pn_type]
+    N, K = w.shape
+    Xd = X.astype(np.float64)
+    H = 2.0 * Xd.T @ Xd
+    H += damp * np.mean(np.diag(H)) * np.eye(K)
+    Hinv = np.linalg.inv(H)
+    W = w.astype(np.float64).copy()
+    out = np.zeros((N, K))
+    d = np.zeros(N, dtype=np.float32)
+    for k in range(K):
+        if k % bpb == 0:
+            blk = W[:, k:k + bpb].astype(np.float32)
+            j = np.argmax(np.abs(blk), axis=1)                  # first index on ties
+            a = blk[np.arange(N), j]
+            d = (a / np.float32(-z)).astype(np.float16).astype(np.float32)
+        v = W[:, k].astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = np.clip(np.rint(v / np.where(d == 0, np.float32(1), d)), -z, z - 1).astype(np.float32)
+        q = np.where(d == 0, np.float32(0), q)
+        wq = (d * q).astype(np.float32).astype(np.float64)
+        out[:, k] = wq
+        err = (W[:, k] - wq) / Hinv[k, k]
+        W[:, k + 1:] -= np.outer(err, Hinv[k, k + 1:])
+        Hinv = Hinv - np.outer(Hinv[:, k], Hinv[k, :]) / Hinv[k, k]
+    return out
+
+
+def pin_gptq_diagonal_is_rtn(o):
+    rng = np.random.default_rng(41)
+    for t in (PN3T, PN4T):
+        bpb = GEOMETRY[t][0]
+        K = 2 * bpb
+        w = (0.02 * rng.standard_normal((5, K))).astype(np.float32)
+        X = np.diag(rng.uniform(0.5, 2.0, K)).astype(np.float32)   # orthogonal columns: H is diagonal
+        assert np.array_equal(o.gptq(t, w, X, 0.01), o.pack(t, w))
+
+
+def pin_gptq_matches_obq(o):
+    rng = np.random.default_rng(42)
+    for t in (PN3T, PN4T):
+        bpb = GEOMETRY[t][0]
+        N, K, n = 6, 2 * bpb, 3 * bpb
+        w = (0.02 * rng.standard_normal((N, K))).astype(np.float32)
+        A = rng.standard_normal((K, K)) * 0.3 + np.eye(K)
+        X = (rng.standard_normal((n, K)) @ A).astype(np.float32)
+        got = o.unpack(t, o.gptq(t, w, X, 0.01), K).astype(np.float64)
+        want = _gptq_reference(t, w, X, 0.01)
+        assert np.array_equal(got, want)
+
+
+def pin_gptq_beats_rtn(o):
+    rng = np.random.default_rng(43)
+    for t in (PN3T, PN4T):
+        bpb = GEOMETRY[t][0]
+        N, K, n = 16, 3 * bpb, 4 * bpb
+        w = (0.02 * rng.standard_normal((N, K))).astype(np.float32)
+        A = rng.standard_normal((K, K)) * 0.5 + np.eye(K)
+        X = (rng.standard_normal((n, K)) @ A).astype(np.float32)
+        e_gptq = np.linalg.norm((w - o.unpack(t, o.gptq(t, w, X, 0.01), K)).astype(np.float64) @ X.T.astype(np.float64))
+        e_rtn = np.linalg.norm((w - o.unpack(t, o.pack(t, w), K)).astype(np.float64) @ X.T.astype(np.float64))
+        assert e_gptq < 0.8 * e_rtn, (e_gptq, e_rtn)
+
+
 ALL_PINS = [pin_block_geometry, pin_worked_blocks, pin_fp16_conversion, pin_decode_exact_all_scales,
             pin_half_structure, pin_every_half_round_trips, pin_full_range_and_bound,
             pin_on_grid_lossless, pin_special_blocks, pin_gemv_exact_tiny, pin_gemv_independent,
             pin_hadamard_worked, pin_hadamard_dense, pin_hadamard_structure,
             pin_unpack_f16_worked, pin_unpack_f16_is_rounded_decode, pin_gemm_f16_exact_tiny,
-            pin_gemm_f16_matches_gemv_on_grid]
+            pin_gemm_f16_matches_gemv_on_grid, pin_gptq_diagonal_is_rtn, pin_gptq_matches_obq,
+            pin_gptq_beats_rtn]
 
 
 # ------------------------------------------------------------------- tests ----
@@ -525,6 +600,14 @@ MUTATIONS = {
                                 "double p = (double)oracle_half_to_float(w16[k * N + n]) * (double)oracle_half_to_float(xrow[k]);"),
     "gemm_fp32_accumulate": ("double sum = 0.0, sum_abs = 0.0;", "float sum = 0.0f; double sum_abs = 0.0;"),
     "gemm_token_zero": ("const uint16_t* xrow = x + (int64_t)m * K;", "const uint16_t* xrow = x;"),
+    "gptq_no_feedback": ("for (int64_t j = k + 1; j < K; ++j) W[r * K + j] -= err * C[j * K + k];",
+                         "for (int64_t j = k + 1; j < K; ++j) W[r * K + j] -= 0.0 * err * C[j * K + k];"),
+    "gptq_factor_of_h": ("if (!cholesky_lower(Hi, C, K))", "if (!cholesky_lower(H, C, K))"),
+    "gptq_transposed_factor": ("W[r * K + j] -= err * C[j * K + k];", "W[r * K + j] -= err * C[k * K + j] + err * C[j * K + k] * (j == k + 1);"),
+    "gptq_scale_from_original": ("cur[j] = (float)W[r * K + b * f.per_block + j];", "cur[j] = w[r * K + b * f.per_block + j];"),
+    "gptq_no_damping": ("H[i * K + i] += damp * mean_diag;", "H[i * K + i] += 1e-9 * damp * mean_diag;"),
+    "gptq_error_not_scaled": ("const double err = (W[r * K + k] - (double)wq) / ukk;",
+                              "const double err = (W[r * K + k] - (double)wq);"),
 }
 
 
