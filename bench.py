@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4, 5, 6])
-    ap.add_argument("--algo", choices=["auto", "tc", "cuda_core"], default="auto")
+    ap.add_argument("--algo", choices=["auto", "tc", "cuda_core", "cuda_core_staged"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -577,7 +577,8 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
     from bit_weight_only_pn_gb300 import pn, synth
     name, tensors, M = workload(cfg, m_override)
     default_m = workload(cfg)[2] == M
-    algo = {"auto": pn.ALGO_AUTO, "tc": pn.ALGO_TENSOR_CORE, "cuda_core": pn.ALGO_CUDA_CORE}[args.algo]
+    algo = {"auto": pn.ALGO_AUTO, "tc": pn.ALGO_TENSOR_CORE, "cuda_core": pn.ALGO_CUDA_CORE,
+            "cuda_core_staged": pn.ALGO_CUDA_CORE_STAGED}[args.algo]
     step_bytes = algorithmic_bytes(tensors, M)
     wbytes = sum(N * (K // per_block(t)) * 34 for t, K, N in tensors)
     copies = max(2, int(np.ceil(ROTATE_BYTES / wbytes)))

@@ -98,12 +98,16 @@ bool tc_eligible(const pn::GemvTensor& t) {
 // Sorts the tensors of a call into the tensor-core and CUDA-core kernels.
 pn_status route(const pn::GemvTensor* ts, int count, int algo, int major, pn::GemvTensor* tc, int* ntc,
                 pn::GemvTensor* simt, int* nsimt) {
-    if (algo != PN_ALGO_AUTO && algo != PN_ALGO_TENSOR_CORE && algo != PN_ALGO_CUDA_CORE) return PN_EINVAL;
+    if (algo != PN_ALGO_AUTO && algo != PN_ALGO_TENSOR_CORE && algo != PN_ALGO_CUDA_CORE &&
+        algo != PN_ALGO_CUDA_CORE_STAGED)
+        return PN_EINVAL;
     *ntc = *nsimt = 0;
     for (int e = 0; e < count; ++e) {
         if (ts[e].N == 0) continue;
         const bool ok_tc = tc_eligible(ts[e]) && major >= 10;
-        if (algo == PN_ALGO_TENSOR_CORE && !ok_tc) return major >= 10 ? PN_EALIGN : PN_EUNSUPPORTED;
+        if ((algo == PN_ALGO_TENSOR_CORE || algo == PN_ALGO_CUDA_CORE_STAGED) && !ok_tc)
+            return major >= 10 ? PN_EALIGN : PN_EUNSUPPORTED;
+        if (algo == PN_ALGO_CUDA_CORE_STAGED && ts[e].nb / 8 > pn::ffma_max_chunks()) return PN_EUNSUPPORTED;
         if (algo != PN_ALGO_CUDA_CORE && ok_tc) tc[(*ntc)++] = ts[e];
         else simt[(*nsimt)++] = ts[e];
     }
@@ -119,6 +123,15 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
     pn::GemvTensor simt[pn::kMaxLayer];
     int ntc = 0, nsimt = 0;
     if ((st = route(ts, count, algo, major, tc, &ntc, simt, &nsimt)) != PN_OK) return st;
+    if (algo == PN_ALGO_CUDA_CORE_STAGED) {
+        if (M > 8) return PN_EUNSUPPORTED;
+        if (ntc == 0) return PN_OK;
+        if (!ws || !aligned(ws, 256)) return PN_EINVAL;
+        if (pn::workspace_layout(sms).total > ws_bytes) return PN_EINVAL;
+        uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws));
+        const cudaError_t e = pn::launch_gemv_ffma(tc, ntc, M, status, sms, g_timeout_ns.load(), s);
+        return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
+    }
     if (ntc > 0) {
         if (!ws || !aligned(ws, 256)) return PN_EINVAL;
         const pn::WorkspaceLayout L = pn::workspace_layout(sms);

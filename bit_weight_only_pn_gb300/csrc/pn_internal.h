@@ -161,6 +161,13 @@ int tc_max_ctas(int num_sms);
 bool tc_split(const GemvTensor* t, int count, int M, int num_sms, int* grid, uint32_t* starts);
 size_t tc_partial_bytes(int num_sms);
 
+// CUDA-core GEMV for 1 <= M <= 8 on the same TMA-staged rows (same
+// eligibility, rows of at most ffma_max_chunks() chunks): the FMA-pipe side
+// of the tensor-core comparison.  Uses only the workspace's status word.
+cudaError_t launch_gemv_ffma(const GemvTensor* t, int count, int M, uint32_t* status, int num_sms,
+                             uint64_t timeout_ns, cudaStream_t s);
+int ffma_max_chunks();
+
 // Host-side checks of a one-tensor GEMV, the same ones pn_gemv_ex makes before
 // it launches anything.  On PN_OK, *uses_workspace tells whether the call
 // would launch a tensor-core kernel (which reads and writes the workspace; the

@@ -14,7 +14,7 @@ import torch
 
 PN3T = 124
 PN4T = 125
-ALGO_AUTO, ALGO_TENSOR_CORE, ALGO_CUDA_CORE = 0, 1, 2
+ALGO_AUTO, ALGO_TENSOR_CORE, ALGO_CUDA_CORE, ALGO_CUDA_CORE_STAGED = 0, 1, 2, 3
 MAX_M = 16
 MAX_LAYER = 8
 STATUS = {0: "PN_OK", 1: "PN_EINVAL", 2: "PN_EALIGN", 3: "PN_EUNSUPPORTED", 4: "PN_ECUDA",

@@ -72,7 +72,13 @@ typedef enum {
 typedef enum {
     PN_ALGO_AUTO = 0,         /* tensor-core kernel where eligible, else CUDA cores */
     PN_ALGO_TENSOR_CORE = 1,  /* TMA-staged rows, decode into mma.sync fragments   */
-    PN_ALGO_CUDA_CORE = 2     /* one lane per code word, fp32 FMAs                 */
+    PN_ALGO_CUDA_CORE = 2,    /* one lane per code word, fp32 FMAs                 */
+    PN_ALGO_CUDA_CORE_STAGED = 3  /* TMA-staged rows as for the tensor cores; each
+                                     decoded fp16 (n - z) times fp16 x added in fp32
+                                     on the FMA pipe (fma.rn.f32.f16) for every
+                                     token; 1 <= M <= 8, rows of at most 64 chunks
+                                     of 8 blocks, tensor-core alignment rules
+                                     (PN_EUNSUPPORTED / PN_EALIGN otherwise) */
 } pn_algo;
 
 #define PN_BLOCK_BYTES 34

@@ -101,17 +101,18 @@ def test_pack_byte_exact(pn, dev, oracle, pn_type):
 SHAPES = [(1000, 8), (16, 8), (17, 16), (129, 24), (300, 40)]   # (N, blocks per row)
 
 
-@pytest.mark.parametrize("algo", ["tc", "cuda_core"])
+@pytest.mark.parametrize("algo", ["tc", "cuda_core", "cuda_core_staged"])
 @pytest.mark.parametrize("pn_type", TYPES)
 def test_gemv_every_m(pn, dev, oracle, pn_type, algo):
-    a = pn.ALGO_TENSOR_CORE if algo == "tc" else pn.ALGO_CUDA_CORE
+    a = {"tc": pn.ALGO_TENSOR_CORE, "cuda_core": pn.ALGO_CUDA_CORE,
+         "cuda_core_staged": pn.ALGO_CUDA_CORE_STAGED}[algo]
     bpb = GEOMETRY[pn_type][0]
     for N, nb in SHAPES:
         K = nb * bpb
         W, x16 = synth_case(oracle, pn_type, N, K, 16, 0x900 + N)
         Wd = to_dev(W, dev)
         ws = pn.Workspace(N, dev)
-        for M in range(1, 17):
+        for M in range(1, 9 if algo == "cuda_core_staged" else 17):
             x = x16[:M]
             y_ref, abs_sum = oracle.gemv(pn_type, W, K, x)
             y = pn.gemv(pn_type, Wd, K, to_dev(x, dev), workspace=ws, algo=a).cpu().numpy()
@@ -312,3 +313,29 @@ def test_gemv_long_rows_one_and_two_tokens(pn, dev, oracle, pn_type):
         assert_gemv_close(entries[0][4].cpu().numpy(), y_ref, abs_sum)
         y2_ref, a2 = oracle.gemv(PN3T, W2, 640, x2)
         assert_gemv_close(entries[1][4].cpu().numpy(), y2_ref, a2)
+
+
+def test_cuda_core_staged_layer_and_limits(pn, dev, oracle):
+    # the FMA-pipe kernel over a mixed layer at M = 8 (every output), and its
+    # refusals: more than 8 tokens, rows longer than 64 chunks
+    shapes = [(PN3T, 640, 300), (PN4T, 512, 129), (PN3T, 1280, 1000), (PN4T, 17408, 77)]
+    M = 8
+    entries, refs = [], []
+    for i, (t, K, N) in enumerate(shapes):
+        W, x = synth_case(oracle, t, N, K, M, 0x7A0 + i)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        entries.append((t, to_dev(W, dev), K, to_dev(x, dev), y))
+        refs.append(oracle.gemv(t, W, K, x))
+    ws = pn.Workspace(sum(s[2] for s in shapes), dev)
+    pn.gemv_layer(entries, M, workspace=ws, algo=pn.ALGO_CUDA_CORE_STAGED)
+    assert ws.status() == 0
+    for (t, Wd, K, xd, y), (y_ref, abs_sum) in zip(entries, refs):
+        assert_gemv_close(y.cpu().numpy(), y_ref, abs_sum)
+    W, x = synth_case(oracle, PN3T, 64, 640, 9, 0x7B0)
+    with pytest.raises(pn.PnError) as err:
+        pn.gemv(PN3T, to_dev(W, dev), 640, to_dev(x, dev), workspace=ws, algo=pn.ALGO_CUDA_CORE_STAGED)
+    assert err.value.status == 3
+    W, x = synth_case(oracle, PN4T, 16, 65 * 512, 1, 0x7B1)
+    with pytest.raises(pn.PnError) as err:
+        pn.gemv(PN4T, to_dev(W, dev), 65 * 512, to_dev(x, dev), workspace=ws, algo=pn.ALGO_CUDA_CORE_STAGED)
+    assert err.value.status == 3

@@ -41,10 +41,11 @@ def to_dev(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
-@pytest.mark.parametrize("algo", ["tc", "cuda_core"])
+@pytest.mark.parametrize("algo", ["tc", "cuda_core", "cuda_core_staged"])
 @pytest.mark.parametrize("pn_type,K", [(PN3T, 5120), (PN4T, 5120), (PN4T, 17408)])
 def test_zero_code_blocks(pn, dev, oracle, pn_type, K, algo):
-    a = pn.ALGO_TENSOR_CORE if algo == "tc" else pn.ALGO_CUDA_CORE
+    a = {"tc": pn.ALGO_TENSOR_CORE, "cuda_core": pn.ALGO_CUDA_CORE,
+         "cuda_core_staged": pn.ALGO_CUDA_CORE_STAGED}[algo]
     bpb = GEOMETRY[pn_type][0]
     N = 1000
     rng = np.random.default_rng(0x2E40 + K + pn_type)
@@ -53,6 +54,8 @@ def test_zero_code_blocks(pn, dev, oracle, pn_type, K, algo):
     Wd = to_dev(W, dev)
     ws = pn.Workspace(N, dev)
     for M in (1, 2, 3, 8, 16):
+        if algo == "cuda_core_staged" and M > 8:
+            continue
         x = x16[:M]
         y_ref, abs_sum = oracle.gemv(pn_type, W, K, x)
         y = pn.gemv(pn_type, Wd, K, to_dev(x, dev), workspace=ws, algo=a).cpu().numpy()
