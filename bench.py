@@ -73,7 +73,13 @@ def parse_args():
     ap.add_argument("--hadamard", type=int, default=0,
                     help="rotate every tensor's activations with pn_hadamard (this block size) "
                          "before its GEMV, inside each step (0 = off)")
-    return ap.parse_args()
+    ap.add_argument("--fused-hadamard", type=int, default=0,
+                    help="GEMV on activations rotated inside the GEMV launch (pn_gemv_hadamard, this "
+                         "block size; M <= 2; 0 = off)")
+    args = ap.parse_args()
+    if args.fused_hadamard and args.hadamard:
+        raise SystemExit("--hadamard and --fused-hadamard are exclusive")
+    return args
 
 
 # ----------------------------------------------------------------- helpers ---
@@ -618,7 +624,13 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
         if xr is not None:
             for (_, _, _, _, xs), xo in zip(sets, xr):
                 pn.hadamard(xs, args.hadamard, out=xo, stream=stream)
-        if len(entries) == 1:
+        if args.fused_hadamard:
+            if len(entries) == 1:
+                t, W, K, x, y = entries[0]
+                pn.gemv_hadamard(t, W, K, x, args.fused_hadamard, y=y, workspace=ws, stream=stream)
+            else:
+                pn.gemv_layer_hadamard(entries, M, args.fused_hadamard, workspace=ws, stream=stream)
+        elif len(entries) == 1:
             t, W, K, x, y = entries[0]
             pn.gemv(t, W, K, x, y=y, workspace=ws, algo=algo, stream=stream)
         else:
@@ -780,7 +792,8 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
     per_gpu = step_bytes / (ms_per_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s",
                 "frac": per_gpu / peak,
-                "traffic": recorded_traffic(cfg) if (default_m and not args.hadamard and args.algo == "auto")
+                "traffic": recorded_traffic(cfg) if (default_m and not args.hadamard and not args.fused_hadamard
+                                                     and args.algo == "auto")
                 else None,
                 "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                if peak_kind == "measured" else "fallback 6.8 TB/s"}
@@ -806,7 +819,7 @@ def run_ours(args, world, rank, local):
     # the metric's other half: the skinny verification batch (M = 8) over the
     # 27B-class layer, timed the same way, in the same line
     m8 = None
-    if not args.no_m8 and args.config != 4 and not args.m:
+    if not args.no_m8 and args.config != 4 and not args.m and not args.fused_hadamard:
         q = measure_gemv(args, 4, 0, world, dev, min(args.e2e_steps, 200))
         m8 = {"workload": q["name"], "M": q["M"], "us_per_gemv": q["ms_per_step"] * 1e3,
               "value": q["value"], "unit": "GB/s", "steps": args.steps, "warmup": args.warmup,
@@ -840,7 +853,8 @@ def run_ours(args, world, rank, local):
                              f"{PREHEAT_S:.1f} s of replays untimed before the timed region",
                    "parallelism": "replicas" if world > 1 else "1 GPU",
                    "algo": args.algo,
-                   "hadamard_block": args.hadamard or None},
+                   "hadamard_block": args.hadamard or None,
+                   "fused_hadamard_block": args.fused_hadamard or None},
         "us_per_gemv": r["ms_per_step"] * 1e3,
         "pct_of_nominal_8tbs": r["per_gpu"] / NOMINAL_HBM_GBS * 100.0,
         "gpu_launches": r["launches"],

@@ -156,6 +156,25 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
     return PN_OK;
 }
 
+// No output of a layer call may overlap another entry's operands or output.
+pn_status check_layer_overlaps(const pn_gemv_desc* descs, int count, int M) {
+    for (int a = 0; a < count; ++a) {
+        if (descs[a].N == 0) continue;
+        const size_t ya = static_cast<size_t>(M) * descs[a].N * 4;
+        for (int b = 0; b < count; ++b) {
+            if (b == a || descs[b].N == 0) continue;
+            const int bpb = per_block(descs[b].type);
+            const size_t wb = static_cast<size_t>(descs[b].N) * (descs[b].K / bpb) * PN_BLOCK_BYTES;
+            const size_t xb = static_cast<size_t>(M) * descs[b].K * 2;
+            const size_t yb = static_cast<size_t>(M) * descs[b].N * 4;
+            if (overlaps(descs[a].y, ya, descs[b].W, wb) || overlaps(descs[a].y, ya, descs[b].x, xb) ||
+                overlaps(descs[a].y, ya, descs[b].y, yb))
+                return PN_EINVAL;
+        }
+    }
+    return PN_OK;
+}
+
 // Checks shared by pn_gemm_f16 and pn_prefill (w16 is the fp16 operand: the
 // caller's matrix or the scratch chunk).
 pn_status check_gemm(int64_t N, int64_t K, const void* x, int64_t M, const float* y, int64_t ldy,
@@ -293,27 +312,75 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
         pn_status st = check_tensor(d.type, d.W, d.N, d.K, d.x, M, d.y, &ts[e]);
         if (st != PN_OK) return st;
     }
-    // No output may overlap another entry's operands or output.
-    for (int a = 0; a < count; ++a) {
-        if (descs[a].N == 0) continue;
-        const size_t ya = static_cast<size_t>(M) * descs[a].N * 4;
-        for (int b = 0; b < count; ++b) {
-            if (b == a || descs[b].N == 0) continue;
-            const int bpb = per_block(descs[b].type);
-            const size_t wb = static_cast<size_t>(descs[b].N) * (descs[b].K / bpb) * PN_BLOCK_BYTES;
-            const size_t xb = static_cast<size_t>(M) * descs[b].K * 2;
-            const size_t yb = static_cast<size_t>(M) * descs[b].N * 4;
-            if (overlaps(descs[a].y, ya, descs[b].W, wb) || overlaps(descs[a].y, ya, descs[b].x, xb) ||
-                overlaps(descs[a].y, ya, descs[b].y, yb))
-                return PN_EINVAL;
-        }
-    }
+    if (pn_status st = check_layer_overlaps(descs, count, M); st != PN_OK) return st;
     return run_layer(ts, count, M, workspace, workspace_bytes, algo, reinterpret_cast<cudaStream_t>(stream));
 }
 
 pn_status pn_gemv_layer(const pn_gemv_desc* descs, int count, int M, void* workspace,
                         size_t workspace_bytes, pn_stream stream) {
     return pn_gemv_layer_ex(descs, count, M, workspace, workspace_bytes, PN_ALGO_AUTO, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// GEMVs of `count` checked tensors on their activations rotated by blocks of
+// `block` (pn_hadamard's arithmetic), in one launch of the one-/two-token
+// kernel, which keeps the rotated activations in shared memory.
+pn_status run_rotated(const pn::GemvTensor* ts, int count, int M, int block, void* ws, size_t ws_bytes,
+                      cudaStream_t s) {
+    if (block < 32 || block > 1024 || (block & (block - 1))) return PN_EINVAL;
+    for (int e = 0; e < count; ++e)
+        if ((static_cast<int64_t>(ts[e].nb) * per_block(ts[e].type)) % block) return PN_EINVAL;
+    int sms = 0, major = 0;
+    pn_status st = device_info(&sms, &major);
+    if (st != PN_OK) return st;
+    pn::GemvTensor live[pn::kMaxLayer];
+    int n = 0;
+    for (int e = 0; e < count; ++e) {
+        if (ts[e].N == 0) continue;
+        if (major < 10) return PN_EUNSUPPORTED;
+        if (!tc_eligible(ts[e])) return PN_EALIGN;
+        if (ts[e].nb / 8 > pn::stream_max_chunks()) return PN_EUNSUPPORTED;
+        live[n++] = ts[e];
+    }
+    if (M > 2) return PN_EUNSUPPORTED;
+    if (n == 0) return PN_OK;
+    if (!pn::stream_rotation_fits(live, n, M, sms, block)) return PN_EUNSUPPORTED;
+    if (!ws || !aligned(ws, 256)) return PN_EINVAL;
+    const pn::WorkspaceLayout L = pn::workspace_layout(sms);
+    if (L.total > ws_bytes) return PN_EINVAL;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const cudaError_t e = pn::launch_gemv_stream(live, n, M, reinterpret_cast<uint32_t*>(base + L.status),
+                                                 reinterpret_cast<uint64_t*>(base + L.tagged), sms,
+                                                 g_timeout_ns.load(), g_test_stall.load(), s, block);
+    return e == cudaSuccess ? PN_OK : pn::cuda_error(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+pn_status pn_gemv_hadamard(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M, int block,
+                           float* y, void* workspace, size_t workspace_bytes, pn_stream stream) {
+    pn::GemvTensor t{};
+    pn_status st = check_tensor(type, W, N, K, x, M, y, &t);
+    if (st != PN_OK) return st;
+    return run_rotated(&t, 1, M, block, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pn_status pn_gemv_layer_hadamard(const pn_gemv_desc* descs, int count, int M, int block, void* workspace,
+                                 size_t workspace_bytes, pn_stream stream) {
+    if (!descs || count < 1 || count > PN_MAX_LAYER) return PN_EINVAL;
+    pn::GemvTensor ts[pn::kMaxLayer];
+    for (int e = 0; e < count; ++e) {
+        const pn_gemv_desc& d = descs[e];
+        pn_status st = check_tensor(d.type, d.W, d.N, d.K, d.x, M, d.y, &ts[e]);
+        if (st != PN_OK) return st;
+    }
+    if (pn_status st = check_layer_overlaps(descs, count, M); st != PN_OK) return st;
+    return run_rotated(ts, count, M, block, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 pn_status pn_hadamard(const uint16_t* x, int M, int64_t K, int block, uint16_t* out, pn_stream stream) {

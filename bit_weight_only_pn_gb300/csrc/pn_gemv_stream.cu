@@ -33,6 +33,15 @@
 // the fifteen consumer warps takes the next stage by ticket, decodes it and
 // frees it, so the block's warps share its units as they become free.
 //
+// Activations.  Staged: each stage carries its unit's activations, as above.
+// Resident (layers and two-token calls, where it fits beside the ring): the
+// producer copies, once per block, the whole activation vectors of the
+// tensors the block's range touches into shared memory, and the stages carry
+// weights only.  Rotated (the fused runtime Hadamard rotation of the
+// tensorless docs, "How Qwen3.8-27B-PN3 uses it"): the consumer warps first
+// rotate those activation vectors into shared memory with pn_hadamard's
+// arithmetic, then decode as in the resident case.
+//
 // Combining.  A unit's partial sums (16 rows x M tokens) go to a slot of a
 // shared-memory ring; a counter per tile counts the units done, and the warp
 // that finishes a tile's last unit adds the tile's partials in chunk order.
@@ -71,7 +80,8 @@ constexpr int kBoxBytes = kRows * kChunkBytes;            // 4352
 constexpr int kStreamMaxM = 2;                            // tokens this kernel serves
 constexpr int kXTokenBytes = kChunkBlocks * 80 * 2;       // 1280: a pn3t chunk of activations (pn4t: 1024)
 constexpr int kStagesLog2 = 5;
-constexpr int kStages = 1 << kStagesLog2;                 // ring stages (a power of two)
+constexpr int kStages = 1 << kStagesLog2;                 // ring stages (a power of two), at most
+constexpr int kMinStagesLog2 = 4;                         // the ring's smallest size (> kConsumers)
 constexpr int kPartsLog2 = 6;
 constexpr int kParts = 1 << kPartsLog2;                   // partial-sum slots in shared memory
 constexpr int kSlotFloats = kRows * kStreamMaxM;          // [row][token]
@@ -81,31 +91,38 @@ constexpr uint64_t kDrainLimitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kStatusTimeout = 5;                    // PN_ETIMEOUT
 constexpr uint32_t kEnd = 0xFFFFFFFFu;                    // tile field of a stage that ends a consumer
 constexpr uint32_t kSuspendNs = 1000;                     // suspend hint of a barrier wait
-static_assert(kStages > kConsumers, "a consumer never waits on a stage two phases ahead");
-static_assert(kStages >= kIssueLanes, "one producer round fits the ring");
+static_assert((1 << kMinStagesLog2) > kConsumers, "a consumer never waits on a stage two phases ahead");
+static_assert((1 << kMinStagesLog2) >= kIssueLanes, "one producer round fits the ring");
 
 __host__ __device__ constexpr int stage_bytes(int M) { return (kBoxBytes + M * kXTokenBytes + 127) / 128 * 128; }
 
-// Shared memory: the ring, one 16-byte unit record per stage, the full and
-// empty barriers, the partial-sum slots with their generation words and tile
-// counters, the ticket counter, the abort flag and zeros.
+// Shared memory: the ring of S stages, one 16-byte unit record per stage, the
+// full and empty barriers, the partial-sum slots with their generation words
+// and tile counters, then either each consumer's copy of a one-token unit's
+// activations (activations staged with the weights) or the activations the
+// block keeps resident (resident_bytes > 0: then the stages hold weights
+// only), the ticket counter, the abort flag, the resident offsets, the
+// resident copy's barrier and zeros.
 struct SmemLayout {
-    int sbytes = 0, table = 0, full = 0, empty = 0, parts = 0, gens = 0, cnts = 0, xown = 0, misc = 0, zeros = 0,
-        total = 0;
-    __host__ __device__ constexpr explicit SmemLayout(int M) {
-        sbytes = stage_bytes(M);
-        table = kStages * sbytes;
-        full = table + 16 * kStages;
-        empty = full + 8 * kStages;
-        parts = empty + 8 * kStages;
+    int sbytes = 0, table = 0, full = 0, empty = 0, parts = 0, gens = 0, cnts = 0, xown = 0, resident = 0,
+        misc = 0, xbar = 0, zeros = 0, total = 0;
+    __host__ __device__ constexpr SmemLayout(int M, int S, uint32_t resident_bytes) {
+        sbytes = resident_bytes ? kBoxBytes : stage_bytes(M);
+        table = S * sbytes;
+        full = table + 16 * S;
+        empty = full + 8 * S;
+        parts = empty + 8 * S;
         gens = parts + kParts * kSlotFloats * 4;
         cnts = gens + 4 * kParts;
-        xown = cnts + 4 * kParts;             // one-token units: each consumer's copy of the activations
-        misc = xown + (M == 1 ? kConsumers * kXTokenBytes : 0);   // ticket (4), abort (4)
-        zeros = (misc + 8 + 15) / 16 * 16;
+        xown = cnts + 4 * kParts;
+        resident = xown + (!resident_bytes && M == 1 ? kConsumers * kXTokenBytes : 0);
+        misc = resident + static_cast<int>((resident_bytes + 15) / 16 * 16);   // ticket (4), abort (4), offsets (32)
+        xbar = misc + 40;
+        zeros = (xbar + 8 + 15) / 16 * 16;
         total = zeros + kZeroBytes;
     }
 };
+constexpr int kSmemLimit = 227 * 1024;
 
 struct STensor {
     const uint16_t* x;
@@ -129,6 +146,15 @@ struct SParams {
     uint64_t* tagged;              // [boundary][kSlotFloats] {tag, value bits}
     uint64_t timeout_ns;
     int stall_first_step;          // testing aid: see pn_set_test_stall
+    int stages_log2;               // the ring holds 1 << stages_log2 stages
+    // rotation of the activations (0 = none): every run of rot_block
+    // activations times H / sqrt(rot_block)
+    int rot_block;
+    float rot_scale;
+    // > 0: every block keeps the activations of the tensors its range
+    // touches in shared memory (rotated if rot_block), this many bytes at
+    // most; 0: each stage carries its unit's activations with its weights
+    uint32_t resident_bytes;
 };
 
 // Tensor, tile and chunk of unit u.
@@ -202,6 +228,11 @@ __device__ __forceinline__ void load_pairs(const uint8_t* p, uint32_t (&v)[NP]) 
 
 __device__ __forceinline__ int lane_id() { return static_cast<int>(threadIdx.x & 31); }
 
+// bar.sync on a named barrier among `threads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ float lds_half(const uint8_t* p) { return __half2float(*reinterpret_cast<const __half*>(p)); }
 
 // Per-unit context of a lane.
@@ -209,7 +240,9 @@ struct Lane {
     int g, t;
     const uint8_t* r0;     // staged row g
     const uint8_t* r1;     // staged row g + 8
-    const uint8_t* x;      // staged activations of token 0 (token m at + m * kXTokenBytes)
+    const uint8_t* x;      // the chunk's activations of token 0 (token m at + m * xstride)
+    int xstride;           // bytes between tokens' activations
+    bool resident;         // x is in the block's resident activations (never overwritten)
     uint8_t* xown;         // this warp's own copy of one token's activations (one-token units)
     const uint8_t* zeros;  // kZeroBytes of zeros
 };
@@ -259,17 +292,21 @@ __device__ __forceinline__ void unit_b8(const Lane& L, int M, float (&acc)[4], R
         d_e1 = half_lo(a1[0]);
         d_o0 = half_hi(a0[8]);
         d_o1 = half_hi(a1[8]);
-        // the chunk's activations (kXTokenBytes at most) to the private copy
+        // the chunk's activations (kXTokenBytes at most) to the private copy,
+        // unless they sit in the block's resident rotated copy
         constexpr int kVec = kChunkBlocks * F::kPerBlock * 2 / 16;
+        if (!L.resident) {
 #pragma unroll
-        for (int i = 0; i < (kVec + 31) / 32; ++i) {
-            const int j = lane_id() + 32 * i;
-            if (j < kVec) *reinterpret_cast<uint4*>(L.xown + 16 * j) = lds_u128(L.x + 16 * j);
+            for (int i = 0; i < (kVec + 31) / 32; ++i) {
+                const int j = lane_id() + 32 * i;
+                if (j < kVec) *reinterpret_cast<uint4*>(L.xown + 16 * j) = lds_u128(L.x + 16 * j);
+            }
         }
     }
     release();                                          // (orders this warp's copy before its reads too)
-    const uint8_t* xo = (g == 2 * t + 1) ? L.xown + (2 * t + 1) * F::kPerBlock * 2 : L.zeros;
-    const uint8_t* xe = (g == 2 * t) ? L.xown + 2 * t * F::kPerBlock * 2 : L.zeros;
+    const uint8_t* xs = L.resident ? L.x : L.xown;
+    const uint8_t* xo = (g == 2 * t + 1) ? xs + (2 * t + 1) * F::kPerBlock * 2 : L.zeros;
+    const uint8_t* xe = (g == 2 * t) ? xs + 2 * t * F::kPerBlock * 2 : L.zeros;
     float c[2][4];
 #pragma unroll
     for (int k = 0; k < 2; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = 0.0f;
@@ -311,7 +348,7 @@ __device__ __forceinline__ void unit_b4(const Lane& L, int M, float (&acc)[4], R
     const uint32_t sel = (t & 1) ? 0x3210u : 0x5432u;
     // column c <-> token c >> 2, block c & 3 of the group; lane t decodes block t
     const bool has_b = (g & 3) == t && (g >> 2) < M;
-    const uint8_t* xt = L.x + (g >> 2) * kXTokenBytes;
+    const uint8_t* xt = L.x + (g >> 2) * L.xstride;
     static_for<2>([&](auto gc) {
         constexpr int G = decltype(gc)::value;
         const int blk = 4 * G + t;
@@ -425,6 +462,79 @@ __device__ __forceinline__ bool smem_wait_eq(const volatile uint32_t* p, uint32_
     }
 }
 
+// --------------------------------------------------------------- rotation --
+//
+// The runtime Hadamard rotation (tensorless docs, "How Qwen3.8-27B-PN3 uses
+// it"), fused: each block rotates the activations of the tensors its range
+// touches once, into shared memory, before its warps decode.  The arithmetic
+// is the one pn_hadamard fixes, so the rotated values are the same bits: fp16
+// -> fp32, butterfly stages h = 1, 2, ..., B/2 in that order, each replacing
+// (v[i], v[i+h]) for (i & h) == 0 by (v[i] + v[i+h], v[i] - v[i+h]) in fp32,
+// one fp32 multiply by the scale, fp16 round-to-nearest-even.  A warp takes
+// one run of B = 32 E activations: lane l holds elements l, l + 32, ...,
+// l + 32 (E - 1), so the stages h < 32 pair lane l with lane l ^ h by shuffle
+// and the stages h >= 32 stay in the lane; every load and store of the warp
+// covers 32 consecutive activations (coalesced, free of bank conflicts).
+
+template <int E>
+__device__ __forceinline__ void rotate_run(const uint16_t* src, uint8_t* dst, float scale, int lane) {
+    float v[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) v[i] = __half2float(__ushort_as_half(src[lane + 32 * i]));
+    // stages h = 1 .. 16 across lanes: the lower lane of a pair keeps
+    // v[j] + v[j + h], the upper one v[j] - v[j + h]
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], h);
+            v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+        }
+    }
+    // stages h = 32 .. B / 2 in the lane: elements i and i + h / 32
+#pragma unroll
+    for (int g = 1; g < E; g <<= 1) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            if (i & g) continue;
+            const float a = v[i], b = v[i + g];
+            v[i] = __fadd_rn(a, b);
+            v[i + g] = __fsub_rn(a, b);
+        }
+    }
+    uint16_t* q = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+    for (int i = 0; i < E; ++i) q[lane + 32 * i] = __half_as_ushort(__float2half_rn(__fmul_rn(v[i], scale)));
+}
+
+// The consumer warps rotate, together, every run of every token of tensors
+// e_lo .. e_hi into the resident region (tensor e's token m at
+// roff[e] + m * K_e * 2 bytes).
+__device__ void rotate_resident(const SParams& P, uint8_t* resident, const uint32_t* roff, int e_lo, int e_hi,
+                                int warp, int lane) {
+    const int B = P.rot_block;
+    int job = 0;
+    for (int e = e_lo; e <= e_hi; ++e) {
+        const STensor& T = P.t[e];
+        const int runs = T.K / B;
+        for (int m = 0; m < P.M; ++m)
+            for (int r = 0; r < runs; ++r, ++job) {
+                if (job % kConsumers != warp) continue;
+                const uint16_t* src = T.x + static_cast<int64_t>(m) * T.K + static_cast<int64_t>(r) * B;
+                uint8_t* dst = resident + roff[e] + (static_cast<size_t>(m) * T.K + static_cast<size_t>(r) * B) * 2;
+                switch (B >> 5) {
+                    case 1: rotate_run<1>(src, dst, P.rot_scale, lane); break;
+                    case 2: rotate_run<2>(src, dst, P.rot_scale, lane); break;
+                    case 4: rotate_run<4>(src, dst, P.rot_scale, lane); break;
+                    case 8: rotate_run<8>(src, dst, P.rot_scale, lane); break;
+                    case 16: rotate_run<16>(src, dst, P.rot_scale, lane); break;
+                    default: rotate_run<32>(src, dst, P.rot_scale, lane); break;
+                }
+            }
+    }
+}
+
 // ----------------------------------------------------------------- kernel --
 
 // Unit record of a stage, written by the producer: the unit's tile and chunk,
@@ -438,10 +548,16 @@ struct Rec {
     uint32_t n_units;
 };
 
-template <int BPM>
+// BPM: blocks per MMA (8: one token, 4: two tokens); SLOG: log2 of the ring's
+// stages; RES: activations resident (P.resident_bytes > 0) or staged.
+template <int BPM, int SLOG, bool RES>
 __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_constant__ SParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemLayout Lay(P.M);
+    const bool rot = RES && P.rot_block != 0;
+    constexpr bool res = RES;
+    const SmemLayout Lay(P.M, 1 << SLOG, RES ? P.resident_bytes : 0u);
+    constexpr int slog = SLOG;
+    constexpr uint32_t smask = (1u << slog) - 1u;
     const uint32_t sbase = smem_addr(smem);
     const uint32_t full0 = sbase + Lay.full, empty0 = sbase + Lay.empty;
     uint32_t* ticket = reinterpret_cast<uint32_t*>(smem + Lay.misc);
@@ -450,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     float* parts = reinterpret_cast<float*>(smem + Lay.parts);
     volatile uint32_t* gens = reinterpret_cast<volatile uint32_t*>(smem + Lay.gens);
     uint32_t* cnts = reinterpret_cast<uint32_t*>(smem + Lay.cnts);
+    uint32_t* roff = reinterpret_cast<uint32_t*>(smem + Lay.misc + 8);    // resident offset per tensor
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // programmatic dependent launch: the next kernel may start now; this one
     // reads weights early but touches activations, outputs and the workspace
@@ -461,10 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         cnts[i] = 0u;
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < (1 << slog); ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
+        mbar_init(sbase + Lay.xbar, 1);
         *ticket = 0u;
         *abort_flag = 0u;
         fence_mbar_init();
@@ -488,15 +606,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         for (int e = lane; e < P.count; e += 32) prefetch_tensormap(&P.wmap[e]);
         const uint32_t total = n + kConsumers;
         bool ok = true;
-        bool waited = false;
+        bool waited = false, x_issued = false;
         uint32_t b0 = 0, filled_mask = 0;             // the last round and which of its lanes filled
         for (; b0 < total; b0 += kIssueLanes) {
             const uint32_t q = b0 + static_cast<uint32_t>(lane);
             bool mine_ok = true, filled = false;
             if (lane < kIssueLanes && q < total) {
-                const uint32_t s = q & (kStages - 1);
-                if (q >= static_cast<uint32_t>(kStages))
-                    mine_ok = thread_wait(empty0 + 8 * s, ((q >> kStagesLog2) - 1) & 1u, P.timeout_ns, abort_flag);
+                const uint32_t s = q & smask;
+                if (q > smask) mine_ok = thread_wait(empty0 + 8 * s, ((q >> slog) - 1) & 1u, P.timeout_ns, abort_flag);
                 if (mine_ok && q < n) {
                     const uint32_t u = q < nr ? c1 - nr + q : c0 + (q - nr);
                     int e, tile, chunk;
@@ -515,18 +632,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                     r.n_units = hi - lo;
                     table[s] = r;
                     const int halves = kChunkBlocks * per_block(T.type);
-                    mbar_arrive_expect_tx(full0 + 8 * s, kBoxBytes + P.M * halves * 2);
+                    // (with resident activations a stage holds weights only)
+                    mbar_arrive_expect_tx(full0 + 8 * s, kBoxBytes + (res ? 0 : P.M * halves * 2));
                     // (testing aid: with stall_first_step the first unit's
                     // bytes are announced but never copied, so its wait can
                     // only time out)
                     if (!(q == 0 && P.stall_first_step)) {
                         tma_load_2d(sbase + s * Lay.sbytes, &P.wmap[e], chunk * kBoxWords, tile * kRows, full0 + 8 * s);
-                        if (!waited) griddep_wait();      // activations may come from the previous kernel
-                        waited = true;
-                        const uint16_t* x = T.x + static_cast<int64_t>(chunk) * halves;
-                        for (int m = 0; m < P.M; ++m)
-                            bulk_g2s(sbase + s * Lay.sbytes + kBoxBytes + m * kXTokenBytes,
-                                     x + static_cast<int64_t>(m) * T.K, halves * 2, full0 + 8 * s);
+                        if (!res) {
+                            if (!waited) griddep_wait();  // activations may come from the previous kernel
+                            waited = true;
+                            const uint16_t* x = T.x + static_cast<int64_t>(chunk) * halves;
+                            for (int m = 0; m < P.M; ++m)
+                                bulk_g2s(sbase + s * Lay.sbytes + kBoxBytes + m * kXTokenBytes,
+                                         x + static_cast<int64_t>(m) * T.K, halves * 2, full0 + 8 * s);
+                        }
                         filled = true;
                     }
                 } else if (mine_ok) {
@@ -537,20 +657,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
             filled_mask = __ballot_sync(0xFFFFFFFFu, filled);
             ok = __all_sync(0xFFFFFFFFu, mine_ok);
             if (!ok) break;
+            if (RES && !rot && b0 == 0 && lane == 0) {
+                // the resident activations, queued behind the first round's
+                // weights only: their offsets, then one bulk copy per tensor
+                // and token (the barrier's completion publishes the offsets)
+                griddep_wait();
+                int e_lo, dummy0, dummy1;
+                locate(P, c0, e_lo, dummy0, dummy1);
+                uint32_t off = 0;
+                for (int e = e_lo; e <= last_e; ++e) {
+                    roff[e] = off;
+                    off += static_cast<uint32_t>(P.M * P.t[e].K * 2);
+                }
+                mbar_arrive_expect_tx(sbase + Lay.xbar, off);
+                for (int e = e_lo; e <= last_e; ++e)
+                    for (int m = 0; m < P.M; ++m)
+                        bulk_g2s(sbase + Lay.resident + roff[e] + static_cast<uint32_t>(m * P.t[e].K * 2),
+                                 P.t[e].x + static_cast<int64_t>(m) * P.t[e].K, static_cast<uint32_t>(P.t[e].K * 2),
+                                 sbase + Lay.xbar);
+                x_issued = true;
+            }
         }
         if (!ok) {
             if (lane == 0) {
                 *abort_flag = 1u;
                 atomicCAS(P.status, 0u, kStatusTimeout);
                 // let every copy this block started land before it can exit:
-                // only the last kStages tickets can have copies in flight, one
+                // only the last S tickets can have copies in flight, one
                 // per stage, each in its stage's latest phase
                 const uint32_t end = b0 + kIssueLanes;
-                for (uint32_t q = end > static_cast<uint32_t>(kStages) ? end - kStages : 0u; q < end && q < n; ++q) {
+                for (uint32_t q = end > smask + 1 ? end - (smask + 1) : 0u; q < end && q < n; ++q) {
                     const bool copied = q < b0 ? !(q == 0 && P.stall_first_step) : ((filled_mask >> (q - b0)) & 1u) != 0u;
-                    if (copied)
-                        thread_wait(full0 + 8 * (q & (kStages - 1)), (q >> kStagesLog2) & 1u, kDrainLimitNs, nullptr);
+                    if (copied) thread_wait(full0 + 8 * (q & smask), (q >> slog) & 1u, kDrainLimitNs, nullptr);
                 }
+                if (x_issued) thread_wait(sbase + Lay.xbar, 0u, kDrainLimitNs, nullptr);
             }
         }
         return;
@@ -558,21 +698,48 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
 
     // ---------------------------------------------------------- consumers --
     griddep_wait();
+    if (rot) {
+        // the rotated activations of the tensors this block's range touches,
+        // resident from here on (the producer streams weights meanwhile)
+        int e_lo, dummy0, dummy1;
+        locate(P, c0, e_lo, dummy0, dummy1);
+        if (warp == 0 && lane == 0) {
+            uint32_t off = 0;
+            for (int e = e_lo; e <= last_e; ++e) {
+                roff[e] = off;
+                off += static_cast<uint32_t>(P.M * P.t[e].K * 2);
+            }
+        }
+        named_barrier_sync(1, kConsumers * 32);
+        rotate_resident(P, smem + Lay.resident, roff, e_lo, last_e, warp, lane);
+        named_barrier_sync(1, kConsumers * 32);
+    } else if (res && !warp_wait(sbase + Lay.xbar, 0u, P.timeout_ns, abort_flag)) {
+        // (the producer's copies of the resident activations land before
+        // the block can exit)
+        if (lane == 0) {
+            *abort_flag = 1u;
+            atomicCAS(P.status, 0u, kStatusTimeout);
+            if (warp == 0) thread_wait(sbase + Lay.xbar, 0u, kDrainLimitNs, nullptr);
+        }
+        return;
+    }
     Lane L;
     L.g = lane >> 2;
     L.t = lane & 3;
     L.zeros = smem + Lay.zeros;
     L.xown = smem + Lay.xown + warp * kXTokenBytes;
+    L.resident = res;
+    L.xstride = kXTokenBytes;
     for (;;) {
         uint32_t k = 0;
         if (lane == 0) k = atomicAdd(ticket, 1u);
         k = __shfl_sync(0xFFFFFFFFu, k, 0);
-        const uint32_t s = k & (kStages - 1);
-        const uint32_t ph = k >> kStagesLog2;
+        const uint32_t s = k & smask;
+        const uint32_t ph = k >> slog;
         // a stage's barriers are waited on by parity, which tells two
-        // consecutive phases apart only: first wait until ticket k - kStages
+        // consecutive phases apart only: first wait until ticket k - S
         // has released the stage, so the full barrier is at most one phase ahead
-        if (k >= static_cast<uint32_t>(kStages) && !warp_wait(empty0 + 8 * s, (ph - 1) & 1u, P.timeout_ns, abort_flag)) {
+        if (k > smask && !warp_wait(empty0 + 8 * s, (ph - 1) & 1u, P.timeout_ns, abort_flag)) {
             if (lane == 0) {
                 *abort_flag = 1u;
                 atomicCAS(P.status, 0u, kStatusTimeout);
@@ -594,7 +761,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         const uint8_t* stage = smem + s * Lay.sbytes;
         L.r0 = stage + L.g * kChunkBytes;
         L.r1 = stage + (L.g + 8) * kChunkBytes;
-        L.x = stage + kBoxBytes;
+        if (res) {
+            const int chunk = static_cast<int>(rec.chunk_e_flags & 0xFFFFFFu);
+            const STensor& Tx = P.t[e];
+            L.x = smem + Lay.resident + roff[e] + static_cast<size_t>(chunk) * kChunkBlocks * per_block(Tx.type) * 2;
+            L.xstride = Tx.K * 2;
+        } else {
+            L.x = stage + kBoxBytes;
+        }
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         auto release = [&] {                              // the stage may be refilled
             __syncwarp();
@@ -689,10 +863,10 @@ bool encode_rows(CUtensorMap* map, const GemvTensor& t) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BPM>
-cudaError_t launch_bpm(const SParams& P, int smem, cudaStream_t s) {
+template <int BPM, int SLOG, bool RES>
+cudaError_t launch_k(const SParams& P, int smem, cudaStream_t s) {
     static std::atomic<uint64_t> smem_set{0};
-    if (cudaError_t e = set_smem_limit_once(gemv_stream_kernel<BPM>, SmemLayout(kStreamMaxM).total, smem_set);
+    if (cudaError_t e = set_smem_limit_once(gemv_stream_kernel<BPM, SLOG, RES>, kSmemLimit, smem_set);
         e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg{};
@@ -705,10 +879,21 @@ cudaError_t launch_bpm(const SParams& P, int smem, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BPM>, P);
+    return cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BPM, SLOG, RES>, P);
 }
 
-static_assert(SmemLayout(kStreamMaxM).total <= 227 * 1024, "the two-token layout fits one SM");
+// The ring has kStagesLog2 stages, or one power of two fewer where rotated
+// activations need the room.
+static_assert(kStagesLog2 == kMinStagesLog2 + 1, "two ring sizes");
+
+template <int BPM>
+cudaError_t launch_bpm(const SParams& P, int smem, cudaStream_t s) {
+    if (!P.resident_bytes) return launch_k<BPM, kStagesLog2, false>(P, smem, s);
+    return P.stages_log2 == kStagesLog2 ? launch_k<BPM, kStagesLog2, true>(P, smem, s)
+                                        : launch_k<BPM, kMinStagesLog2, true>(P, smem, s);
+}
+
+static_assert(SmemLayout(kStreamMaxM, kStages, 0).total <= kSmemLimit, "the two-token layout fits one SM");
 
 }  // namespace
 
@@ -720,8 +905,19 @@ size_t stream_tagged_bytes(int num_sms) {
     return static_cast<size_t>(stream_max_ctas(num_sms) + 1) * kSlotFloats * sizeof(uint64_t);
 }
 
+// The resident activations a rotating call keeps in a block whose range is
+// [u0, u1): every token's K of each tensor the range touches.
+static uint32_t resident_need(const STensor* T, int count, int M, uint32_t u0, uint32_t u1) {
+    uint32_t bytes = 0;
+    for (int e = 0; e < count; ++e) {
+        const uint32_t b = T[e].unit_base, end = b + static_cast<uint32_t>(T[e].chunks) * T[e].tiles;
+        if (u0 < end && u1 > b) bytes += static_cast<uint32_t>(M) * T[e].K * 2;
+    }
+    return bytes;
+}
+
 cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* status, uint64_t* tagged,
-                               int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s) {
+                               int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s, int rot_block) {
     if (M < 1 || M > kStreamMaxM || count < 1 || count > kMaxLayer) return cudaErrorInvalidValue;
     SParams P{};
     uint64_t units = 0;
@@ -739,6 +935,7 @@ cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* 
         if (!encode_rows(&P.wmap[e], t[e])) return cudaErrorInvalidValue;
         // a tile's chunk partials must all fit the shared-memory slot ring
         if (T.chunks > kParts) return cudaErrorInvalidValue;
+        if (rot_block && T.K % rot_block) return cudaErrorInvalidValue;
         units += static_cast<uint64_t>(T.chunks) * T.tiles;
         max_chunks = T.chunks > max_chunks ? T.chunks : max_chunks;
     }
@@ -757,8 +954,63 @@ cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* 
     P.tagged = tagged;
     P.timeout_ns = timeout_ns;
     P.stall_first_step = stall;
-    const int smem = SmemLayout(M).total;
+    P.stages_log2 = kStagesLog2;
+    uint32_t need = 0;
+    for (int c = 0; c < P.grid; ++c) {
+        const uint32_t b = resident_need(P.t, count, M, P.starts[c], P.starts[c + 1]);
+        need = b > need ? b : need;
+    }
+    if (rot_block) {
+        int m = 0;
+        while ((1 << m) < rot_block) ++m;
+        if ((1 << m) != rot_block || rot_block < 32 || rot_block > 1024) return cudaErrorInvalidValue;
+        const float sqrt2 = 1.41421356237309504880f;
+        P.rot_block = rot_block;
+        P.rot_scale = (m % 2) ? ldexpf(sqrt2, -(m + 1) / 2) : ldexpf(1.0f, -(m / 2));
+        // a smaller ring leaves more room for the rotated activations
+        P.resident_bytes = need;
+        while (SmemLayout(M, 1 << P.stages_log2, need).total > kSmemLimit && P.stages_log2 > kMinStagesLog2)
+            --P.stages_log2;
+        if (SmemLayout(M, 1 << P.stages_log2, need).total > kSmemLimit) return cudaErrorInvalidValue;
+    } else if ((count > 1 || M > 1) && SmemLayout(M, 1 << P.stages_log2, need).total <= kSmemLimit) {
+        // the activations resident beside a full ring, copied in once per
+        // block instead of once per unit.  Measured on GB300 (CUDA-event
+        // timed graph replays): 2.3 us faster on the 27B-class layer at
+        // M = 1, 0.2 us on single tensors at M = 2, but 1.2 to 1.6 us slower
+        // on single tensors at M = 1, where every block copies the same
+        // activations at the same moment; those stay staged.
+        P.resident_bytes = need;
+    }
+    const int smem = SmemLayout(M, 1 << P.stages_log2, P.resident_bytes).total;
     return M == 1 ? launch_bpm<8>(P, smem, s) : launch_bpm<4>(P, smem, s);
+}
+
+bool stream_rotation_fits(const GemvTensor* t, int count, int M, int num_sms, int rot_block) {
+    if (M < 1 || M > kStreamMaxM || count < 1 || count > kMaxLayer || rot_block < 32 || rot_block > 1024 ||
+        (rot_block & (rot_block - 1)))
+        return false;
+    STensor T[kMaxLayer] = {};
+    uint64_t units = 0;
+    int max_chunks = 1;
+    CostSplit split{};
+    for (int e = 0; e < count; ++e) {
+        T[e].K = t[e].nb * per_block(t[e].type);
+        T[e].chunks = t[e].nb / kChunkBlocks;
+        T[e].tiles = (t[e].N + kRows - 1) / kRows;
+        T[e].unit_base = static_cast<uint32_t>(units);
+        if (t[e].nb % kChunkBlocks || T[e].chunks > kParts || T[e].K % rot_block) return false;
+        units += static_cast<uint64_t>(T[e].chunks) * T[e].tiles;
+        max_chunks = T[e].chunks > max_chunks ? T[e].chunks : max_chunks;
+        split.add(static_cast<uint32_t>(T[e].chunks) * T[e].tiles, 1u);
+    }
+    if (units == 0) return true;
+    const int grid = split.fit_grid(stream_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
+    uint32_t need = 0;
+    for (int c = 0; c < grid; ++c) {
+        const uint32_t b = resident_need(T, count, M, split.start(c), split.start(c + 1));
+        need = b > need ? b : need;
+    }
+    return SmemLayout(M, 1 << kMinStagesLog2, need).total <= kSmemLimit;
 }
 
 }  // namespace pn

@@ -143,8 +143,14 @@ WorkspaceLayout workspace_layout(int num_sms);
 // Tensor-core GEMV for M <= 2 over `count` tensors (every one with nb % 8 == 0
 // and W, x 16-byte aligned): one block per SM streams a contiguous range of
 // units through a TMA ring that its warps share.
+// With rot_block (32 .. 1024, a power of two dividing every K) the kernel
+// first rotates each tensor's activations as pn_hadamard would (fused) and
+// multiplies the rotated values; 0 = no rotation.
 cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* status, uint64_t* tagged,
-                               int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s);
+                               int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s, int rot_block = 0);
+// Whether a fused-rotation call on these tensors fits the kernel's shared
+// memory (the rotated activations of a block's tensors stay resident).
+bool stream_rotation_fits(const GemvTensor* t, int count, int M, int num_sms, int rot_block);
 int stream_max_ctas(int num_sms);
 size_t stream_tagged_bytes(int num_sms);
 // Longest row (in 8-block chunks) the one-/two-token kernel takes.

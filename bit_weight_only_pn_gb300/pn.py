@@ -74,6 +74,10 @@ def lib() -> ctypes.CDLL:
             L.pn_gemv_ex.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp, sz, i32, vp]
             L.pn_gemv_layer.restype = i32
             L.pn_gemv_layer.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, vp]
+            L.pn_gemv_hadamard.restype = i32
+            L.pn_gemv_hadamard.argtypes = [i32, vp, i64, i64, vp, i32, i32, vp, vp, sz, vp]
+            L.pn_gemv_layer_hadamard.restype = i32
+            L.pn_gemv_layer_hadamard.argtypes = [ctypes.POINTER(_Desc), i32, i32, i32, vp, sz, vp]
             L.pn_gemv_layer_ex.restype = i32
             L.pn_gemv_layer_ex.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, i32, vp]
             L.pn_unpack_f16.restype = i32
@@ -211,6 +215,38 @@ def gemv_layer(entries, M: int, workspace: Workspace | None = None, algo: int = 
     ws_ptr, ws_bytes = (workspace.ptr, workspace.nbytes) if workspace is not None else (None, 0)
     _check(lib().pn_gemv_layer_ex(arr, len(entries), M, ws_ptr, ws_bytes, algo, _stream(stream)),
            "pn_gemv_layer")
+    return [e[4] for e in entries]
+
+
+def gemv_hadamard(pn_type: int, W: torch.Tensor, K: int, x: torch.Tensor, block: int,
+                  y: torch.Tensor | None = None, workspace: Workspace | None = None, stream=None) -> torch.Tensor:
+    """y = decode(W) @ hadamard(x, block)^T in one launch (see pn_gemv_hadamard)."""
+    _require(W, torch.uint8, "W")
+    _require(x, torch.float16, "x")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    M, N = x.shape[0], W.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=W.device)
+    _require(y, torch.float32, "y")
+    ws_ptr, ws_bytes = (workspace.ptr, workspace.nbytes) if workspace is not None else (None, 0)
+    _check(lib().pn_gemv_hadamard(pn_type, _ptr(W), N, K, _ptr(x), M, block, _ptr(y), ws_ptr, ws_bytes,
+                                  _stream(stream)), "pn_gemv_hadamard")
+    return y
+
+
+def gemv_layer_hadamard(entries, M: int, block: int, workspace: Workspace | None = None, stream=None):
+    """Several independent GEMVs on rotated activations in one launch (see pn_gemv_layer_hadamard)."""
+    entries = list(entries)
+    arr = (_Desc * len(entries))()
+    for i, (t, W, K, x, y) in enumerate(entries):
+        _require(W, torch.uint8, "W")
+        _require(x, torch.float16, "x")
+        _require(y, torch.float32, "y")
+        arr[i] = _Desc(t, _ptr(W), W.shape[0], K, _ptr(x), _ptr(y))
+    ws_ptr, ws_bytes = (workspace.ptr, workspace.nbytes) if workspace is not None else (None, 0)
+    _check(lib().pn_gemv_layer_hadamard(arr, len(entries), M, block, ws_ptr, ws_bytes, _stream(stream)),
+           "pn_gemv_layer_hadamard")
     return [e[4] for e in entries]
 
 

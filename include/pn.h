@@ -231,6 +231,25 @@ pn_status pn_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const u
 pn_status pn_hadamard(const uint16_t* x, int M, int64_t K, int block, uint16_t* out, pn_stream stream);
 
 /*
+ * pn_gemv_hadamard / pn_gemv_layer_hadamard: pn_gemv / pn_gemv_layer on the
+ * activations rotated as pn_hadamard rotates them (runs of `block`, same
+ * arithmetic, so the multiplied fp16 values are exactly pn_hadamard's
+ * output), in one launch: the rotation is fused into the GEMV (tensorless
+ * docs, "How Qwen3.8-27B-PN3 uses it": the engine applies the rotation at
+ * run time).  x is read, not modified.  Limits of the fused path: 1 <= M <= 2;
+ * block a power of two from 32 to 1024 dividing every K (else PN_EINVAL);
+ * the tensor-core alignment rules and rows of at most 64 chunks of 8 blocks
+ * (else PN_EALIGN / PN_EUNSUPPORTED); the rotated activations of the tensors
+ * one SM works on must fit its shared memory (about 70 K activations per
+ * token pair; else PN_EUNSUPPORTED).  Outside these limits, call pn_hadamard
+ * and then pn_gemv.  Same workspace, result and tolerance as pn_gemv.
+ */
+pn_status pn_gemv_hadamard(int type, const void* W, int64_t N, int64_t K, const uint16_t* x, int M, int block,
+                           float* y, void* workspace, size_t workspace_bytes, pn_stream stream);
+pn_status pn_gemv_layer_hadamard(const pn_gemv_desc* descs, int count, int M, int block, void* workspace,
+                                 size_t workspace_bytes, pn_stream stream);
+
+/*
  * Prefill (large M).  The pages' engine dequantizes the weights for prefill
  * and runs a chunked GEMM, rebuilding weights transiently from the packed
  * codes without keeping them (tensorless docs, "What the fork adds";

@@ -107,6 +107,30 @@ def test_hadamard_checks(lib):
     assert h(FAKE, 1, 96, 32, FAKE + 64, None) == PN_EINVAL
 
 
+def test_fused_hadamard_checks(lib):
+    # checks that come before any device query or launch
+    g = lib.pn_gemv_hadamard
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    ws = FAKE * 8
+    for block in (16, 96, 2048, 4096, 0, -32):                    # out of range, not 2^k, not dividing K
+        assert g(124, FAKE, 16, 5120, FAKE * 2, 1, block, FAKE * 4, ws, 1 << 20, None) == PN_EINVAL
+    assert g(124, FAKE, 16, 5120, FAKE * 2, 0, 1024, FAKE * 4, ws, 1 << 20, None) == PN_EINVAL     # M = 0
+    assert g(124, FAKE, 16, 5121, FAKE * 2, 1, 1024, FAKE * 4, ws, 1 << 20, None) == PN_EINVAL     # K
+    assert g(124, FAKE, 16, 5120, FAKE * 2 + 1, 1, 1024, FAKE * 4, ws, 1 << 20, None) == PN_EALIGN
+    assert g(124, FAKE, 16, 5120, FAKE * 2, 1, 1024, FAKE + 64, ws, 1 << 20, None) == PN_EINVAL    # y on W
+    from bit_weight_only_pn_gb300.pn import _Desc
+    arr = (_Desc * 2)()
+    arr[0] = _Desc(124, FAKE, 32, 5120, FAKE * 2, FAKE * 4)
+    arr[1] = _Desc(125, FAKE * 8, 32, 6144, FAKE * 16, FAKE * 4 + 64)    # y overlaps entry 0's y
+    L = lib.pn_gemv_layer_hadamard
+    assert L(arr, 2, 1, 1024, FAKE * 32, 1 << 20, None) == PN_EINVAL
+    arr[1] = _Desc(125, FAKE * 8, 32, 6144, FAKE * 16, FAKE * 64)
+    assert L(arr, 2, 1, 4096, FAKE * 32, 1 << 20, None) == PN_EINVAL    # 4096 divides neither K
+    assert L(arr, 0, 1, 1024, FAKE * 32, 1 << 20, None) == PN_EINVAL
+
+
 def test_prefill_checks(lib):
     # checks that come before any device query or launch
     u, g, p = lib.pn_unpack_f16, lib.pn_gemm_f16, lib.pn_prefill

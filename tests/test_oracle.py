@@ -576,7 +576,7 @@ MUTATIONS = {
     "zero_point_sign": ("out[k] = d * (float)(n - f->zero);", "out[k] = d * (float)(n + f->zero);"),
     "zero_point_value": ("f->per_block = 80; f->per_word = 10; f->bits = 3; f->zero = 4;",
                          "f->per_block = 80; f->per_word = 10; f->bits = 3; f->zero = 3;"),
-    "tie_last_index": ("if (fabsf(v[j]) > amax)", "if (fabsf(v[j]) >= amax)"),
+    "tie_last_index": ("++j) {\n        if (fabsf(v[j]) > amax)", "++j) {\n        if (fabsf(v[j]) >= amax)"),
     "unsigned_step": ("float d32 = a / (float)(-z);", "float d32 = a / (float)(z);"),
     "truncating_codes": ("float q = rintf(v[k] / d);", "float q = truncf(v[k] / d);"),
     "fp16_ties_away": ("if (rem > 0x1000u || (rem == 0x1000u && (r & 1u))) r++;", "if (rem >= 0x1000u) r++;"),
