@@ -38,9 +38,9 @@
 // producer copies, once per block, the whole activation vectors of the
 // tensors the block's range touches into shared memory, and the stages carry
 // weights only.  Rotated (the fused runtime Hadamard rotation of the
-// tensorless docs, "How Qwen3.8-27B-PN3 uses it"): the consumer warps first
-// rotate those activation vectors into shared memory with pn_hadamard's
-// arithmetic, then decode as in the resident case.
+// tensorless docs, "How Qwen3.8-27B-PN3 uses it"): the producer copies them
+// in the same way, the consumer warps rotate them in place with
+// pn_hadamard's arithmetic, then decode as in the resident case.
 //
 // Combining.  A unit's partial sums (16 rows x M tokens) go to a slot of a
 // shared-memory ring; a counter per tile counts the units done, and the warp
@@ -72,6 +72,7 @@ constexpr int kConsumers = 15;                            // decoding warps
 constexpr int kProducerWarp = kConsumers;
 constexpr int kThreads = (kConsumers + 1) * 32;           // 512
 constexpr int kIssueLanes = 16;                           // producer lanes issuing copies at once
+constexpr int kResidentLead = 4;                          // stages requested before resident activations
 constexpr int kRows = 16;                                 // weight rows per tile
 constexpr int kChunkBlocks = 8;
 constexpr int kChunkBytes = kChunkBlocks * kBlockBytes;   // 272
@@ -471,67 +472,83 @@ __device__ __forceinline__ bool smem_wait_eq(const volatile uint32_t* p, uint32_
 // -> fp32, butterfly stages h = 1, 2, ..., B/2 in that order, each replacing
 // (v[i], v[i+h]) for (i & h) == 0 by (v[i] + v[i+h], v[i] - v[i+h]) in fp32,
 // one fp32 multiply by the scale, fp16 round-to-nearest-even.  A warp takes
-// one run of B = 32 E activations: lane l holds elements l, l + 32, ...,
-// l + 32 (E - 1), so the stages h < 32 pair lane l with lane l ^ h by shuffle
-// and the stages h >= 32 stay in the lane; every load and store of the warp
-// covers 32 consecutive activations (coalesced, free of bank conflicts).
+// a job of 64 Q activations (one run of B = 64 Q, or two runs when B = 32):
+// lane l holds the pairs 2l + 64i, 2l + 64i + 1 (i < Q), so stage h = 1 stays
+// in the lane, the stages h = 2 .. 32 pair lane l with lane l ^ (h / 2) by
+// shuffle, and the stages h >= 64 pair its i with i + h / 64.  Across lanes
+// the lower lane keeps v + o and the upper one o - v, both as one
+// fma(+-1, v, o): the product is exact, so the single rounding gives the
+// same bits as the add or subtract.  Loads and stores are 32-bit (a pair).
 
-template <int E>
-__device__ __forceinline__ void rotate_run(const uint16_t* src, uint8_t* dst, float scale, int lane) {
-    float v[E];
+template <int Q>
+__device__ __forceinline__ void rotate_job(uint32_t* job, int B, float scale, int lane) {
+    float v[2 * Q];
 #pragma unroll
-    for (int i = 0; i < E; ++i) v[i] = __half2float(__ushort_as_half(src[lane + 32 * i]));
-    // stages h = 1 .. 16 across lanes: the lower lane of a pair keeps
-    // v[j] + v[j + h], the upper one v[j] - v[j + h]
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-        const bool upper = (lane & h) != 0;
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-            const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], h);
-            v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
-        }
+    for (int i = 0; i < Q; ++i) {
+        const uint32_t w = job[lane + 32 * i];
+        v[2 * i] = half_lo(w);
+        v[2 * i + 1] = half_hi(w);
     }
-    // stages h = 32 .. B / 2 in the lane: elements i and i + h / 32
 #pragma unroll
-    for (int g = 1; g < E; g <<= 1) {
+    for (int i = 0; i < Q; ++i) {                       // h = 1
+        const float a = v[2 * i], b = v[2 * i + 1];
+        v[2 * i] = __fadd_rn(a, b);
+        v[2 * i + 1] = __fsub_rn(a, b);
+    }
+#pragma unroll 1
+    for (int d = 1; d <= 16 && 2 * d < B; d <<= 1) {   // h = 2d, while h < B
+        const float sgn = (lane & d) ? -1.0f : 1.0f;
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
+        for (int j = 0; j < 2 * Q; ++j) v[j] = __fmaf_rn(sgn, v[j], __shfl_xor_sync(0xFFFFFFFFu, v[j], d));
+    }
+#pragma unroll
+    for (int g = 1; g < Q; g <<= 1) {                   // h = 64 g
+#pragma unroll
+        for (int i = 0; i < Q; ++i) {
             if (i & g) continue;
-            const float a = v[i], b = v[i + g];
-            v[i] = __fadd_rn(a, b);
-            v[i + g] = __fsub_rn(a, b);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const float a = v[2 * i + c], b = v[2 * (i + g) + c];
+                v[2 * i + c] = __fadd_rn(a, b);
+                v[2 * (i + g) + c] = __fsub_rn(a, b);
+            }
         }
     }
-    uint16_t* q = reinterpret_cast<uint16_t*>(dst);
 #pragma unroll
-    for (int i = 0; i < E; ++i) q[lane + 32 * i] = __half_as_ushort(__float2half_rn(__fmul_rn(v[i], scale)));
+    for (int i = 0; i < Q; ++i) {
+        const uint32_t lo = __half_as_ushort(__float2half_rn(__fmul_rn(v[2 * i], scale)));
+        const uint32_t hi = __half_as_ushort(__float2half_rn(__fmul_rn(v[2 * i + 1], scale)));
+        job[lane + 32 * i] = lo | (hi << 16);
+    }
 }
 
-// The consumer warps rotate, together, every run of every token of tensors
-// e_lo .. e_hi into the resident region (tensor e's token m at
-// roff[e] + m * K_e * 2 bytes).
-__device__ void rotate_resident(const SParams& P, uint8_t* resident, const uint32_t* roff, int e_lo, int e_hi,
-                                int warp, int lane) {
-    const int B = P.rot_block;
-    int job = 0;
-    for (int e = e_lo; e <= e_hi; ++e) {
-        const STensor& T = P.t[e];
-        const int runs = T.K / B;
-        for (int m = 0; m < P.M; ++m)
-            for (int r = 0; r < runs; ++r, ++job) {
-                if (job % kConsumers != warp) continue;
-                const uint16_t* src = T.x + static_cast<int64_t>(m) * T.K + static_cast<int64_t>(r) * B;
-                uint8_t* dst = resident + roff[e] + (static_cast<size_t>(m) * T.K + static_cast<size_t>(r) * B) * 2;
-                switch (B >> 5) {
-                    case 1: rotate_run<1>(src, dst, P.rot_scale, lane); break;
-                    case 2: rotate_run<2>(src, dst, P.rot_scale, lane); break;
-                    case 4: rotate_run<4>(src, dst, P.rot_scale, lane); break;
-                    case 8: rotate_run<8>(src, dst, P.rot_scale, lane); break;
-                    case 16: rotate_run<16>(src, dst, P.rot_scale, lane); break;
-                    default: rotate_run<32>(src, dst, P.rot_scale, lane); break;
-                }
-            }
+// The consumer warps rotate, together and in place, every run of every token
+// of tensors e_lo .. e_hi in the resident region (tensor e's token m at
+// roff[e] + m * K_e * 2 bytes).  Lane e of every warp holds K_e in k_lane
+// (read from the kernel parameters before the activations are waited for).
+__device__ void rotate_resident(uint8_t* resident, const uint32_t* roff, int e_lo, int e_hi, int M, int B,
+                                float scale, int k_lane, int warp, int lane) {
+    const int q = B >= 64 ? B / 64 : 1;                 // pairs per lane
+    const int job_elems = 64 * q;
+    // jobs are numbered over (tensor, token, offset); this warp takes jobs
+    // warp, warp + kConsumers, ... (e, base: the first job of tensor e)
+    int e = e_lo, base = 0;
+    int K = __shfl_sync(0xFFFFFFFFu, k_lane, e);
+    for (int job = warp;; job += kConsumers) {
+        while (job - base >= M * (K / job_elems)) {
+            base += M * (K / job_elems);
+            if (++e > e_hi) return;
+            K = __shfl_sync(0xFFFFFFFFu, k_lane, e);
+        }
+        const int j = job - base;                         // token-major within the tensor
+        uint32_t* p = reinterpret_cast<uint32_t*>(resident + roff[e]) + static_cast<size_t>(j) * job_elems / 2;
+        switch (q) {
+            case 1: rotate_job<1>(p, B, scale, lane); break;
+            case 2: rotate_job<2>(p, B, scale, lane); break;
+            case 4: rotate_job<4>(p, B, scale, lane); break;
+            case 8: rotate_job<8>(p, B, scale, lane); break;
+            default: rotate_job<16>(p, B, scale, lane); break;
+        }
     }
 }
 
@@ -608,10 +625,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         bool ok = true;
         bool waited = false, x_issued = false;
         uint32_t b0 = 0, filled_mask = 0;             // the last round and which of its lanes filled
-        for (; b0 < total; b0 += kIssueLanes) {
+        // (with resident activations the first round is short, so that the
+        // activations are requested behind a few stages of weights only)
+        uint32_t width = RES ? kResidentLead : kIssueLanes;
+        for (; b0 < total; b0 += width, width = kIssueLanes) {
             const uint32_t q = b0 + static_cast<uint32_t>(lane);
             bool mine_ok = true, filled = false;
-            if (lane < kIssueLanes && q < total) {
+            if (lane < width && q < total) {
                 const uint32_t s = q & smask;
                 if (q > smask) mine_ok = thread_wait(empty0 + 8 * s, ((q >> slog) - 1) & 1u, P.timeout_ns, abort_flag);
                 if (mine_ok && q < n) {
@@ -657,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
             filled_mask = __ballot_sync(0xFFFFFFFFu, filled);
             ok = __all_sync(0xFFFFFFFFu, mine_ok);
             if (!ok) break;
-            if (RES && !rot && b0 == 0 && lane == 0) {
+            if (RES && b0 == 0 && lane == 0) {
                 // the resident activations, queued behind the first round's
                 // weights only: their offsets, then one bulk copy per tensor
                 // and token (the barrier's completion publishes the offsets)
@@ -685,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                 // let every copy this block started land before it can exit:
                 // only the last S tickets can have copies in flight, one
                 // per stage, each in its stage's latest phase
-                const uint32_t end = b0 + kIssueLanes;
+                const uint32_t end = b0 + width;
                 for (uint32_t q = end > smask + 1 ? end - (smask + 1) : 0u; q < end && q < n; ++q) {
                     const bool copied = q < b0 ? !(q == 0 && P.stall_first_step) : ((filled_mask >> (q - b0)) & 1u) != 0u;
                     if (copied) thread_wait(full0 + 8 * (q & smask), (q >> slog) & 1u, kDrainLimitNs, nullptr);
@@ -697,23 +717,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     }
 
     // ---------------------------------------------------------- consumers --
-    griddep_wait();
+    // (what the rotation reads of the parameters, loaded before the waits so
+    // that their latency overlaps them: lane e holds tensor e's K and first
+    // unit)
+    int rot_k = 0, rot_b = 0;
+    uint32_t rot_base = 0;
+    float rot_scale = 0.0f;
     if (rot) {
-        // the rotated activations of the tensors this block's range touches,
-        // resident from here on (the producer streams weights meanwhile)
-        int e_lo, dummy0, dummy1;
-        locate(P, c0, e_lo, dummy0, dummy1);
-        if (warp == 0 && lane == 0) {
-            uint32_t off = 0;
-            for (int e = e_lo; e <= last_e; ++e) {
-                roff[e] = off;
-                off += static_cast<uint32_t>(P.M * P.t[e].K * 2);
-            }
+        rot_b = P.rot_block;
+        rot_scale = P.rot_scale;
+        if (lane < P.count) {
+            rot_k = P.t[lane].K;
+            rot_base = P.t[lane].unit_base;
         }
-        named_barrier_sync(1, kConsumers * 32);
-        rotate_resident(P, smem + Lay.resident, roff, e_lo, last_e, warp, lane);
-        named_barrier_sync(1, kConsumers * 32);
-    } else if (res && !warp_wait(sbase + Lay.xbar, 0u, P.timeout_ns, abort_flag)) {
+    }
+    griddep_wait();
+    if (res && !warp_wait(sbase + Lay.xbar, 0u, P.timeout_ns, abort_flag)) {
         // (the producer's copies of the resident activations land before
         // the block can exit)
         if (lane == 0) {
@@ -722,6 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
             if (warp == 0) thread_wait(sbase + Lay.xbar, 0u, kDrainLimitNs, nullptr);
         }
         return;
+    }
+    if (rot) {
+        // rotate the resident activations in place (the producer streams
+        // weights meanwhile), then every warp may read them
+        // the first tensor of the range: the last whose first unit is <= c0
+        const int e_lo = __popc(__ballot_sync(0xFFFFFFFFu, lane >= 1 && lane < P.count && c0 >= rot_base));
+        rotate_resident(smem + Lay.resident, roff, e_lo, last_e, P.M, rot_b, rot_scale, rot_k, warp, lane);
+        named_barrier_sync(1, kConsumers * 32);
     }
     Lane L;
     L.g = lane >> 2;
