@@ -143,6 +143,12 @@ pn_status run_layer(const pn::GemvTensor* ts, int count, int M, void* ws, size_t
         // thread blocks share each staged activation chunk among eight tiles
         bool stream = M <= 2;
         for (int i = 0; i < ntc; ++i) stream = stream && tc[i].nb / 8 <= pn::stream_max_chunks();
+        // two tokens over several tensors: the one-token kernel only where it
+        // keeps their activations resident (measured on GB300: 16.3 against
+        // 20.5 us on two pn3t tensors whose activations fit; 37.9 against
+        // 38.0 and 48.9 against 41.8 us on sets that do not fit, the
+        // 27B-class layer the latter)
+        if (stream && M == 2 && ntc > 1 && !pn::stream_resident_fits(tc, ntc, M, sms)) stream = false;
         cudaError_t e = stream
             ? pn::launch_gemv_stream(tc, ntc, M, status, reinterpret_cast<uint64_t*>(base + L.tagged), sms,
                                      g_timeout_ns.load(), g_test_stall.load(), s)

@@ -1012,10 +1012,12 @@ cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* 
     return M == 1 ? launch_bpm<8>(P, smem, s) : launch_bpm<4>(P, smem, s);
 }
 
-bool stream_rotation_fits(const GemvTensor* t, int count, int M, int num_sms, int rot_block) {
-    if (M < 1 || M > kStreamMaxM || count < 1 || count > kMaxLayer || rot_block < 32 || rot_block > 1024 ||
-        (rot_block & (rot_block - 1)))
-        return false;
+namespace {
+
+// The largest resident set of any block of a launch over these tensors (0 if
+// the call has no units or does not suit the kernel).
+uint32_t max_resident_need(const GemvTensor* t, int count, int M, int num_sms, int rot_block) {
+    if (M < 1 || M > kStreamMaxM || count < 1 || count > kMaxLayer) return 0;
     STensor T[kMaxLayer] = {};
     uint64_t units = 0;
     int max_chunks = 1;
@@ -1025,19 +1027,32 @@ bool stream_rotation_fits(const GemvTensor* t, int count, int M, int num_sms, in
         T[e].chunks = t[e].nb / kChunkBlocks;
         T[e].tiles = (t[e].N + kRows - 1) / kRows;
         T[e].unit_base = static_cast<uint32_t>(units);
-        if (t[e].nb % kChunkBlocks || T[e].chunks > kParts || T[e].K % rot_block) return false;
+        if (t[e].nb % kChunkBlocks || T[e].chunks > kParts || (rot_block && T[e].K % rot_block)) return 0;
         units += static_cast<uint64_t>(T[e].chunks) * T[e].tiles;
         max_chunks = T[e].chunks > max_chunks ? T[e].chunks : max_chunks;
         split.add(static_cast<uint32_t>(T[e].chunks) * T[e].tiles, 1u);
     }
-    if (units == 0) return true;
+    if (units == 0) return 0;
     const int grid = split.fit_grid(stream_max_ctas(num_sms), static_cast<uint32_t>(max_chunks));
     uint32_t need = 0;
     for (int c = 0; c < grid; ++c) {
         const uint32_t b = resident_need(T, count, M, split.start(c), split.start(c + 1));
         need = b > need ? b : need;
     }
-    return SmemLayout(M, 1 << kMinStagesLog2, need).total <= kSmemLimit;
+    return need;
+}
+
+}  // namespace
+
+bool stream_rotation_fits(const GemvTensor* t, int count, int M, int num_sms, int rot_block) {
+    if (rot_block < 32 || rot_block > 1024 || (rot_block & (rot_block - 1))) return false;
+    const uint32_t need = max_resident_need(t, count, M, num_sms, rot_block);
+    return need > 0 && SmemLayout(M, 1 << kMinStagesLog2, need).total <= kSmemLimit;
+}
+
+bool stream_resident_fits(const GemvTensor* t, int count, int M, int num_sms) {
+    const uint32_t need = max_resident_need(t, count, M, num_sms, 0);
+    return need > 0 && SmemLayout(M, 1 << kStagesLog2, need).total <= kSmemLimit;
 }
 
 }  // namespace pn

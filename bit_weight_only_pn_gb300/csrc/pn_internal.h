@@ -148,6 +148,9 @@ WorkspaceLayout workspace_layout(int num_sms);
 // multiplies the rotated values; 0 = no rotation.
 cudaError_t launch_gemv_stream(const GemvTensor* t, int count, int M, uint32_t* status, uint64_t* tagged,
                                int num_sms, uint64_t timeout_ns, int stall, cudaStream_t s, int rot_block = 0);
+// Whether a call on these tensors keeps their activations resident in the
+// one-/two-token kernel's shared memory beside its full ring.
+bool stream_resident_fits(const GemvTensor* t, int count, int M, int num_sms);
 // Whether a fused-rotation call on these tensors fits the kernel's shared
 // memory (the rotated activations of a block's tensors stay resident).
 bool stream_rotation_fits(const GemvTensor* t, int count, int M, int num_sms, int rot_block);

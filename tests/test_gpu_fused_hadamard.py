@@ -9,8 +9,9 @@ uses it") instead of in a separate pn_hadamard launch.  Three checks:
   encodes exactly) every output y[m][j] is one rotated activation times 1.0
   plus zeros, so y equals the oracle's rotation exactly (as values: the sign
   of a zero may differ);
-* y bit-identical to pn_hadamard followed by pn_gemv on the same device (same
-  kernel, same split, same summation order), for single tensors and layers;
+* y bit-identical to pn_hadamard followed by pn_gemv on the same device where
+  both run the same kernel (same split, same summation order): single tensors
+  and one-token layers;
 * y within the GEMV tolerance of the oracle's rotation followed by the
   oracle's GEMV.
 
@@ -111,9 +112,15 @@ def test_fused_layer(pn, oracle, M, block):
     assert ws.status() == 0
     for (t, W, K, x), e, f in zip(host, ents, two):
         y = e[4].cpu().numpy()
-        assert np.array_equal(y.view(np.uint32), f[4].cpu().numpy().view(np.uint32))
         y_ref, abs_sum = oracle.gemv(t, W, K, oracle.hadamard(x, block))
         assert_gemv_close(y, y_ref, abs_sum)
+        if M == 1:
+            # same kernel, split and order as the two-launch path (at M = 2
+            # this layer's two-launch GEMV runs the batch kernel instead,
+            # whose sums are ordered differently)
+            assert np.array_equal(y.view(np.uint32), f[4].cpu().numpy().view(np.uint32))
+        else:
+            assert_gemv_close(f[4].cpu().numpy(), y_ref, abs_sum)
 
 
 def test_fused_full_size_layer_sampled(pn, oracle):
