@@ -26,8 +26,8 @@
 
 namespace {
 
-// Room for the workspace of a device with up to 203 SMs (the workspace size
-// depends only on the SM count: about 2.5 KiB per SM).
+// Room for the workspace of a device with up to 226 SMs (the workspace size
+// depends only on the SM count: about 2.3 KiB per SM).
 constexpr size_t kNoAllocScratchBytes = 512 * 1024;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

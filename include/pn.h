@@ -126,7 +126,7 @@ pn_status pn_unpack(int type, const void* W, int64_t N, int64_t K, float* w, pn_
  * them, which adds the other block's part in a fixed order, so results are
  * deterministic.  That needs device scratch: a status word and, per
  * thread-block boundary, hand-off slots and a counter.  The size depends only
- * on the device's SM count (about 2.5 KiB per SM), so calls of any shape can
+ * on the device's SM count (about 2.3 KiB per SM), so calls of any shape can
  * share one workspace.
  *
  * pn_workspace_bytes(total_rows): bytes needed by one call whose tensors have
@@ -192,7 +192,7 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
  *
  * Scratch: a fixed 512 KiB array in the library's device image, which every
  * GPU that loads the library holds until the process exits.  A device whose
- * workspace (pn_workspace_bytes) would not fit (more than 203 SMs) gets
+ * workspace (pn_workspace_bytes) would not fit (more than 226 SMs) gets
  * PN_EINVAL and nothing is launched.  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress, which may load the
  * library's device module); make that first call before capturing a stream

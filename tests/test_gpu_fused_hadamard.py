@@ -178,3 +178,33 @@ def test_fused_refusals(pn, oracle):
     assert err.value.status == EUNSUPPORTED
     torch.cuda.synchronize()
     assert ws.status() == 0
+
+
+@pytest.mark.parametrize("rotated", [False, True])
+def test_resident_wait_timeout_reports_status(pn, oracle, rotated):
+    # A layer call (activations resident, rotated or copied) whose first weight
+    # copy is announced but never made (testing aid): the waits give up after
+    # the limit, the blocks let their other copies land, PN_ETIMEOUT is
+    # reported, and the next call on the same workspace is right.
+    shapes = [(PN3T, 5120, 640), (PN4T, 6144, 320)]
+    ents, host = layer_case(oracle, 1, shapes, 0xFD0 + rotated)
+    ws = pn.Workspace(sum(e[1].shape[0] for e in ents), dev())
+    call = (lambda: pn.gemv_layer_hadamard(ents, 1, 1024, workspace=ws)) if rotated else \
+        (lambda: pn.gemv_layer(ents, 1, workspace=ws))
+    try:
+        pn.set_wait_timeout_ns(2_000_000)
+        pn.set_test_stall(True)
+        call()
+        assert ws.status() == 5
+    finally:
+        pn.set_test_stall(False)
+        pn.set_wait_timeout_ns(1_000_000_000)
+    for e in ents:
+        e[4].fill_(float("nan"))
+    call()
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    for (t, W, K, x), e in zip(host, ents):
+        xr = oracle.hadamard(x, 1024) if rotated else x
+        y_ref, abs_sum = oracle.gemv(t, W, K, xr)
+        assert_gemv_close(e[4].cpu().numpy(), y_ref, abs_sum)
