@@ -37,6 +37,24 @@
 namespace pn {
 namespace {
 
+// The same copy with an L2 eviction policy (a createpolicy value) for the
+// lines it reads.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int x, int y, uint32_t bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
+}
+
+// L2 policy: keep the lines this thread reads (evict them last).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+
 // ------------------------------------------------------------- unpack f16 --
 
 template <int TYPE>
@@ -238,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
             // ------------------------------------------------------ producer --
             int it = 0;                       // K slices issued, over all tiles
             bool stop = false;
+            // the activations are read again for every weight-row tile: keep
+            // them in L2 (the weight rows are read by the 16 token tiles of a
+            // row tile at about the same time, and y is written streaming)
+            const uint64_t keep = l2_policy_evict_last();
             for (int t = blockIdx.x; t < P.tiles && !stop; t += gridDim.x) {
                 const int tok0 = (t % P.tiles_tok) * kTileTokens;
                 const int row0 = (t / P.tiles_tok) * kTileRows;
@@ -258,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
                     // time out)
                     if (!(P.stall_first_step && it == 0)) {
                         tma_load_2d(a, &P.amap, kb * kKStep, row0, full(s));
-                        tma_load_2d(a + kABytes, &P.bmap, kb * kKStep, tok0, full(s));
+                        tma_load_2d_hint(a + kABytes, &P.bmap, kb * kKStep, tok0, full(s), keep);
                     }
                     ++it;
                 }
@@ -337,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
                     float* yc = P.y + static_cast<int64_t>(tok0 + c) * P.ldy + row;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (tok0 + c + j < P.M) yc[static_cast<int64_t>(j) * P.ldy] = __uint_as_float(v[j]);
+                        if (tok0 + c + j < P.M) __stcs(yc + static_cast<int64_t>(j) * P.ldy, __uint_as_float(v[j]));
                 }
             }
             tc_fence_before_sync();
