@@ -208,3 +208,14 @@ def test_resident_wait_timeout_reports_status(pn, oracle, rotated):
         xr = oracle.hadamard(x, 1024) if rotated else x
         y_ref, abs_sum = oracle.gemv(t, W, K, xr)
         assert_gemv_close(e[4].cpu().numpy(), y_ref, abs_sum)
+
+
+def test_fused_empty_rows(pn, oracle):
+    # N = 0 is a no-op that returns PN_OK and writes nothing
+    W, x = tensor_case(oracle, PN3T, 16, 5120, 1, 0xFE0)
+    xd = torch.from_numpy(x).to(dev())
+    Wd = torch.from_numpy(W).to(dev())[:0]
+    y = torch.full((1, 1), 7.0, dtype=torch.float32, device=dev())
+    pn.gemv_hadamard(PN3T, Wd, 5120, xd, 1024, y=y[:, :0], workspace=pn.Workspace(16, dev()))
+    torch.cuda.synchronize()
+    assert y.item() == 7.0
