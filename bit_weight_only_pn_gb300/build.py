@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libpn_gb300.so")
 SOURCES = ["pn_capi.cu", "pn_codec.cu", "pn_gemv_ffma.cu", "pn_gemv_simt.cu", "pn_gemv_stream.cu", "pn_gemv_tc.cu",
-           "pn_noalloc.cu", "pn_prefill.cu", "pn_probe.cu", "pn_rotate.cu"]
+           "pn_gptq.cu", "pn_noalloc.cu", "pn_prefill.cu", "pn_probe.cu", "pn_rotate.cu"]
 HEADERS = ["pn_device.cuh", "pn_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

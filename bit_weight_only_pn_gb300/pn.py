@@ -74,6 +74,10 @@ def lib() -> ctypes.CDLL:
             L.pn_gemv_ex.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp, sz, i32, vp]
             L.pn_gemv_layer.restype = i32
             L.pn_gemv_layer.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, sz, vp]
+            L.pn_gptq_scratch_bytes.restype = sz
+            L.pn_gptq_scratch_bytes.argtypes = [i64, i64]
+            L.pn_gptq.restype = i32
+            L.pn_gptq.argtypes = [i32, vp, i64, i64, vp, i64, ctypes.c_double, vp, vp, sz, vp]
             L.pn_gemv_hadamard.restype = i32
             L.pn_gemv_hadamard.argtypes = [i32, vp, i64, i64, vp, i32, i32, vp, vp, sz, vp]
             L.pn_gemv_layer_hadamard.restype = i32
@@ -248,6 +252,26 @@ def gemv_layer_hadamard(entries, M: int, block: int, workspace: Workspace | None
     _check(lib().pn_gemv_layer_hadamard(arr, len(entries), M, block, ws_ptr, ws_bytes, _stream(stream)),
            "pn_gemv_layer_hadamard")
     return [e[4] for e in entries]
+
+
+def gptq(pn_type: int, w: torch.Tensor, X: torch.Tensor, damp: float = 0.01, stream=None) -> torch.Tensor:
+    """GPTQ-style quantisation (see pn_gptq): fp32 w [N][K] and calibration
+    inputs X fp32 [n][K] -> PN rows [N][row_bytes].  Synchronous."""
+    _require(w, torch.float32, "w")
+    _require(X, torch.float32, "X")
+    N, K = w.shape
+    if X.dim() != 2 or X.shape[1] != K:
+        raise ValueError("X must be [n][K]")
+    rb = row_bytes(pn_type, K)
+    if rb == 0:
+        raise ValueError("K is not a whole number of blocks")
+    W = torch.empty((N, rb), dtype=torch.uint8, device=w.device)
+    nbytes = int(lib().pn_gptq_scratch_bytes(N, K))
+    scratch = torch.empty(nbytes + 256, dtype=torch.uint8, device=w.device)
+    base = (scratch.data_ptr() + 255) // 256 * 256
+    _check(lib().pn_gptq(pn_type, _ptr(w), N, K, _ptr(X), X.shape[0], float(damp), _ptr(W), base, nbytes,
+                         _stream(stream)), "pn_gptq")
+    return W
 
 
 def hadamard(x: torch.Tensor, block: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

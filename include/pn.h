@@ -250,6 +250,28 @@ pn_status pn_gemv_layer_hadamard(const pn_gemv_desc* descs, int count, int M, in
                                  size_t workspace_bytes, pn_stream stream);
 
 /*
+ * pn_gptq: GPTQ-style quantisation of fp32 weights w [N][K] into PN rows
+ * W [N][pn_row_bytes(type, K)] (tensorless docs, "How Qwen3.8-27B-PN3 uses
+ * it": the weights were quantised "GPTQ-style").  The published GPTQ
+ * (Frantar et al., ICLR 2023, Algorithm 1) with the PN blocks as its groups:
+ * H = 2 X^T X + lambda I over calibration inputs X fp32 [n][K] (lambda = damp
+ * times the mean of diag(2 X^T X), damp > 0, typically 0.01); U the upper
+ * Cholesky factor of H^-1; columns in order, each row's block scale taken by
+ * the signed-scale rule from the block's current weights when the block
+ * starts, each column rounded with that scale and its error / U[k][k] fed to
+ * the later columns through U's row k.  fp64 throughout (fp32 for the scale
+ * and the rounding), each sum in index order, so the bytes equal the CPU
+ * oracle's.  Synchronous (returns when W is written).  scratch: device,
+ * 256-byte aligned, pn_gptq_scratch_bytes(N, K) bytes (4 K^2 + N K doubles).
+ * w and X 4-byte aligned, W any alignment.  PN_EINVAL for bad sizes, a small
+ * scratch, or a Hessian that is not positive definite; N = 0 does nothing.
+ * Not part of the GEMV's path: an offline tool, quadratic in K.
+ */
+size_t pn_gptq_scratch_bytes(int64_t N, int64_t K);
+pn_status pn_gptq(int type, const float* w, int64_t N, int64_t K, const float* X, int64_t n, double damp,
+                  void* W, void* scratch, size_t scratch_bytes, pn_stream stream);
+
+/*
  * Prefill (large M).  The pages' engine dequantizes the weights for prefill
  * and runs a chunked GEMM, rebuilding weights transiently from the packed
  * codes without keeping them (tensorless docs, "What the fork adds";

@@ -131,6 +131,28 @@ def test_fused_hadamard_checks(lib):
     assert L(arr, 0, 1, 1024, FAKE * 32, 1 << 20, None) == PN_EINVAL
 
 
+def test_gptq_checks(lib):
+    # checks that come before any device work
+    g = lib.pn_gptq
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    sb = lib.pn_gptq_scratch_bytes
+    sb.restype = ctypes.c_size_t
+    sb.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    need = sb(8, 160)
+    assert need >= (4 * 160 * 160 + 8 * 160) * 8 and sb(8, 0) == 0 and sb(-1, 160) == 0
+    ws = FAKE * 64
+    assert g(7, FAKE, 8, 160, FAKE * 2, 10, 0.01, FAKE * 4, ws, need, None) == PN_EINVAL      # type
+    assert g(124, FAKE, 8, 161, FAKE * 2, 10, 0.01, FAKE * 4, ws, need, None) == PN_EINVAL    # K
+    assert g(124, FAKE, 8, 160, FAKE * 2, 0, 0.01, FAKE * 4, ws, need, None) == PN_EINVAL     # n
+    assert g(124, FAKE, 8, 160, FAKE * 2, 10, 0.0, FAKE * 4, ws, need, None) == PN_EINVAL     # damp
+    assert g(124, FAKE, 8, 160, FAKE * 2, 10, 0.01, FAKE * 4, ws, need - 1, None) == PN_EINVAL  # scratch
+    assert g(124, FAKE + 2, 8, 160, FAKE * 2, 10, 0.01, FAKE * 4, ws, need, None) == PN_EALIGN
+    assert g(124, FAKE, 8, 160, FAKE * 2, 10, 0.01, FAKE * 4, ws + 16, need, None) == PN_EALIGN
+    assert g(124, FAKE, 0, 160, FAKE * 2, 10, 0.01, FAKE * 4, ws, need, None) == 0            # nothing to do
+
+
 def test_prefill_checks(lib):
     # checks that come before any device query or launch
     u, g, p = lib.pn_unpack_f16, lib.pn_gemm_f16, lib.pn_prefill
