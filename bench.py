@@ -76,6 +76,9 @@ def parse_args():
     ap.add_argument("--fused-hadamard", type=int, default=0,
                     help="GEMV on activations rotated inside the GEMV launch (pn_gemv_hadamard, this "
                          "block size; M <= 2; 0 = off)")
+    ap.add_argument("--gptq", action="store_true",
+                    help="time the device GPTQ-style quantiser (pn_gptq) on the workload's first tensor "
+                         "with 256 calibration rows, and the oracle on a small sample")
     args = ap.parse_args()
     if args.fused_hadamard and args.hadamard:
         raise SystemExit("--hadamard and --fused-hadamard are exclusive")
@@ -869,12 +872,70 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_gptq(args, world, rank):
+    """The offline quantiser (pn_gptq), not the GEMV: seconds per tensor on the
+    device, and device against oracle on a small sample (K = 640, 64 rows)."""
+    import numpy as np
+    import torch
+    from bit_weight_only_pn_gb300 import build, pn, synth
+    if rank != 0:
+        return
+    build.build()
+    dev = torch.device("cuda", 0)
+    t, K, N = synth.CONFIGS[args.config]["tensors"][0]
+    n = 256
+
+    def inputs(N, K, seed):
+        rng = np.random.default_rng(seed)
+        w = synth.weights(synth.weight_seed(args.config, 0), N, K)
+        A = rng.standard_normal((K, K)) * (0.3 / np.sqrt(K / 64)) + np.eye(K)
+        X = (rng.standard_normal((n, K)) @ A).astype(np.float32)
+        return w, X
+
+    def time_device(w, X, reps):
+        wd, Xd = torch.from_numpy(w).to(dev), torch.from_numpy(X).to(dev)
+        pn.gptq(t, wd, Xd)                                    # warm-up (module load, allocations)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            W = pn.gptq(t, wd, Xd)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps, W
+
+    w, X = inputs(N, K, 1)
+    full_s, _ = time_device(w, X, max(1, min(args.steps, 3)))
+    ws, Xs = inputs(64, 640, 2)
+    small_s, Wsmall = time_device(ws, Xs, 3)
+    o = None
+    oracle_s = None
+    try:
+        import oracle as oracle_mod
+        o = oracle_mod.Oracle()
+        t0 = time.perf_counter()
+        want = o.gptq(t, ws, Xs, 0.01)
+        oracle_s = time.perf_counter() - t0
+        same = bool(np.array_equal(Wsmall.cpu().numpy(), want))
+    except Exception as e:                                    # the oracle is optional here
+        same = f"oracle unavailable: {e}"
+    flops = 2.0 * N * K * K / 2 + 4.0 * K ** 3 / 3 + 2.0 * n * K * K
+    print(json.dumps({
+        "metric": "PN GPTQ-style quantisation time (device, offline tool)", "value": full_s, "unit": "s",
+        "higher_is_better": False, "n_gpus": 1, "steps": max(1, min(args.steps, 3)), "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{'pn3t' if t == 124 else 'pn4t'} {K}->{N}, "
+                                                   f"{n} calibration rows", "parallelism": "1 GPU"},
+        "fp64_gflop": flops / 1e9, "fp64_gflops_achieved": flops / full_s / 1e9,
+        "small_sample": {"workload": f"K=640, 64 rows, {n} calibration rows", "device_s": small_s,
+                         "oracle_s": oracle_s, "bytes_equal_oracle": same}}))
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup(args)
     from bit_weight_only_pn_gb300 import synth
     prefill = synth.CONFIGS[args.config].get("prefill", False)
-    if args.impl == "reference":
+    if args.gptq:
+        run_gptq(args, world, rank)
+    elif args.impl == "reference":
         run_reference_prefill(args, world, rank) if prefill else run_reference(args, world, rank)
     elif prefill:
         run_prefill(args, world, rank, local)

@@ -18,8 +18,9 @@
 // in fp64 (fp32 for the scale and the rounding, as the format's own rule).
 // Every floating-point step here is one IEEE operation with round-to-nearest
 // (explicit _rn intrinsics, so nothing is fused), in the order above, so the
-// result does not depend on how the work is spread over threads: each sum is
-// taken in index order by one thread.  Rows are independent given U, so the
+// result does not depend on how the work is spread over threads: products may
+// be formed in parallel, but each sum adds its terms in index order.  Rows
+// are independent given U, so the
 // quantisation runs one thread block per group of rows; the factorisations
 // run column by column, each column's entries in parallel.
 //
@@ -60,12 +61,39 @@ __global__ void damp_kernel(double* __restrict__ H, int64_t K, double damp) {
     for (int64_t i = 0; i < K; ++i) H[i * K + i] = __dadd_rn(H[i * K + i], __dmul_rn(damp, m));
 }
 
-// Cholesky a = c c^T, column j: the pivot (one thread) ...
+// Cholesky a = c c^T, column j.  The sums keep the sequential order (k =
+// 0, 1, ...); what runs in parallel is the loading and the products.  fp64 is
+// slow on this part, so each subtraction is done once, by the thread that
+// owns the sum.  The pivot: one block; products in shared memory by tiles,
+// one thread subtracts them ...
+constexpr int kPivotTile = 2048;
+constexpr int kUnroll = 8;
+
 __global__ void chol_pivot_kernel(const double* __restrict__ a, double* __restrict__ c, int64_t K, int64_t j,
                                   uint32_t* __restrict__ failed) {
-    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    __shared__ double prod[kPivotTile];
     double s = a[j * K + j];
-    for (int64_t k = 0; k < j; ++k) s = __dsub_rn(s, __dmul_rn(c[j * K + k], c[j * K + k]));
+    for (int64_t k0 = 0; k0 < j; k0 += kPivotTile) {
+        const int n = static_cast<int>(j - k0 < kPivotTile ? j - k0 : kPivotTile);
+        for (int q = threadIdx.x; q < n; q += blockDim.x) {
+            const double v = c[j * K + k0 + q];
+            prod[q] = __dmul_rn(v, v);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int q = 0;
+            for (; q + kUnroll <= n; q += kUnroll) {
+                double p[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) p[u] = prod[q + u];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) s = __dsub_rn(s, p[u]);
+            }
+            for (; q < n; ++q) s = __dsub_rn(s, prod[q]);
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x != 0) return;
     if (!(s > 0.0)) {
         *failed = 1u;
         s = 1.0;                        // keeps the rest finite; the call reports the failure
@@ -73,29 +101,72 @@ __global__ void chol_pivot_kernel(const double* __restrict__ a, double* __restri
     c[j * K + j] = __dsqrt_rn(s);
 }
 
-// ... and the entries below it, one thread per row i > j.
-__global__ void chol_column_kernel(const double* __restrict__ a, double* __restrict__ c, int64_t K, int64_t j) {
-    const int64_t i = j + 1 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (i >= K) return;
-    double t = a[i * K + j];
-    for (int64_t k = 0; k < j; ++k) t = __dsub_rn(t, __dmul_rn(c[i * K + k], c[j * K + k]));
-    c[i * K + j] = __ddiv_rn(t, c[j * K + j]);
+// ... and the entries below it, one thread per row i > j; each block stages
+// 32-column slices of its rows and of row j in shared memory (coalesced
+// loads), and every thread subtracts its row's products in order.
+constexpr int kColThreads = 32;
+
+__global__ void __launch_bounds__(kColThreads) chol_column_kernel(const double* __restrict__ a,
+                                                                  double* __restrict__ c, int64_t K, int64_t j) {
+    __shared__ double tile[kColThreads][33];
+    __shared__ double cj[32];
+    const int64_t i0 = j + 1 + static_cast<int64_t>(blockIdx.x) * kColThreads;
+    const int64_t i = i0 + threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    double t = i < K ? a[i * K + j] : 0.0;
+    for (int64_t k0 = 0; k0 < j; k0 += 32) {
+        const int n = static_cast<int>(j - k0 < 32 ? j - k0 : 32);
+        // warp w loads rows i0 + w, w + 4, ...: lane = column within the slice
+        for (int r = warp; r < kColThreads; r += kColThreads / 32) {
+            const int64_t row = i0 + r;
+            tile[r][lane] = (row < K && lane < n) ? c[row * K + k0 + lane] : 0.0;
+        }
+        if (threadIdx.x < 32) cj[threadIdx.x] = lane < n ? c[j * K + k0 + lane] : 0.0;
+        __syncthreads();
+        if (i < K)
+            for (int q = 0; q < n; ++q) t = __dsub_rn(t, __dmul_rn(tile[threadIdx.x][q], cj[q]));
+        __syncthreads();
+    }
+    if (i < K) c[i * K + j] = __ddiv_rn(t, c[j * K + j]);
 }
 
 // inv = a^-1 from a = c c^T, one thread per column: c y = e_col by forward
 // substitution, then c^T x = y by back substitution.  y lives in tmp[i][col].
+// The operands of kUnroll terms are loaded before they are subtracted in order.
 __global__ void spd_inverse_kernel(const double* __restrict__ c, double* __restrict__ inv,
                                    double* __restrict__ tmp, int64_t K) {
     const int64_t col = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if (col >= K) return;
     for (int64_t i = 0; i < K; ++i) {
         double s = (i == col) ? 1.0 : 0.0;
-        for (int64_t k = 0; k < i; ++k) s = __dsub_rn(s, __dmul_rn(c[i * K + k], tmp[k * K + col]));
+        int64_t k = 0;
+        for (; k + kUnroll <= i; k += kUnroll) {
+            double cv[kUnroll], tv[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                cv[u] = c[i * K + k + u];
+                tv[u] = tmp[(k + u) * K + col];
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) s = __dsub_rn(s, __dmul_rn(cv[u], tv[u]));
+        }
+        for (; k < i; ++k) s = __dsub_rn(s, __dmul_rn(c[i * K + k], tmp[k * K + col]));
         tmp[i * K + col] = __ddiv_rn(s, c[i * K + i]);
     }
     for (int64_t i = K - 1; i >= 0; --i) {
         double s = tmp[i * K + col];
-        for (int64_t k = i + 1; k < K; ++k) s = __dsub_rn(s, __dmul_rn(c[k * K + i], inv[k * K + col]));
+        int64_t k = i + 1;
+        for (; k + kUnroll <= K; k += kUnroll) {
+            double cv[kUnroll], iv[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                cv[u] = c[(k + u) * K + i];
+                iv[u] = inv[(k + u) * K + col];
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) s = __dsub_rn(s, __dmul_rn(cv[u], iv[u]));
+        }
+        for (; k < K; ++k) s = __dsub_rn(s, __dmul_rn(c[k * K + i], inv[k * K + col]));
         inv[i * K + col] = __ddiv_rn(s, c[i * K + i]);
     }
 }
@@ -245,8 +316,10 @@ extern "C" pn_status pn_gptq(int type, const float* w, int64_t N, int64_t K, con
     uint32_t* failed = reinterpret_cast<uint32_t*>(base + L.flag);
     auto chol = [&](const double* a, double* c) {
         for (int64_t j = 0; j < K; ++j) {
-            pn::chol_pivot_kernel<<<1, 1, 0, s>>>(a, c, K, j, failed);
-            if (K - j - 1 > 0) pn::chol_column_kernel<<<pn::blocks_for(K - j - 1, 128), 128, 0, s>>>(a, c, K, j);
+            pn::chol_pivot_kernel<<<1, 256, 0, s>>>(a, c, K, j, failed);
+            if (K - j - 1 > 0)
+                pn::chol_column_kernel<<<pn::blocks_for(K - j - 1, pn::kColThreads), pn::kColThreads, 0, s>>>(a, c,
+                                                                                                         K, j);
         }
     };
     cudaError_t e = cudaMemsetAsync(failed, 0, sizeof(uint32_t), s);
@@ -254,7 +327,7 @@ extern "C" pn_status pn_gptq(int type, const float* w, int64_t N, int64_t K, con
     pn::hessian_kernel<<<pn::blocks_for(K * K, 256), 256, 0, s>>>(X, n, K, H);
     pn::damp_kernel<<<1, 1, 0, s>>>(H, K, damp);
     chol(H, C);
-    pn::spd_inverse_kernel<<<pn::blocks_for(K, 64), 64, 0, s>>>(C, Hi, U, K);
+    pn::spd_inverse_kernel<<<pn::blocks_for(K, 32), 32, 0, s>>>(C, Hi, U, K);
     chol(Hi, C);
     pn::transpose_lower_kernel<<<pn::blocks_for(K * K, 256), 256, 0, s>>>(C, U, K);
     pn::widen_kernel<<<pn::blocks_for(N * K, 256) < 4096 ? pn::blocks_for(N * K, 256) : 4096, 256, 0, s>>>(
