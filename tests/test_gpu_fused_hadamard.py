@@ -219,3 +219,29 @@ def test_fused_empty_rows(pn, oracle):
     pn.gemv_hadamard(PN3T, Wd, 5120, xd, 1024, y=y[:, :0], workspace=pn.Workspace(16, dev()))
     torch.cuda.synchronize()
     assert y.item() == 7.0
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_layer_whose_activations_do_not_fit(pn, oracle, M):
+    # three short 17408-wide tensors: a block's range spans all of them, whose
+    # activations (M x 3 x 34 KB) do not fit beside the full ring, so the
+    # one-token launch stages them per unit (M = 1) or the call goes to the
+    # batch kernel (M = 2); the fused-rotation call still fits at M = 1
+    shapes = [(PN4T, 17408, 40), (PN4T, 17408, 24), (PN4T, 17408, 33)]
+    ents, host = layer_case(oracle, M, shapes, 0xFF0 + M)
+    ws = pn.Workspace(200, dev())
+    pn.gemv_layer(ents, M, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    for (t, W, K, x), e in zip(host, ents):
+        y_ref, abs_sum = oracle.gemv(t, W, K, x)
+        assert_gemv_close(e[4].cpu().numpy(), y_ref, abs_sum)
+    if M == 1:
+        for e in ents:
+            e[4].fill_(float("nan"))
+        pn.gemv_layer_hadamard(ents, M, 1024, workspace=ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        for (t, W, K, x), e in zip(host, ents):
+            y_ref, abs_sum = oracle.gemv(t, W, K, oracle.hadamard(x, 1024))
+            assert_gemv_close(e[4].cpu().numpy(), y_ref, abs_sum)
