@@ -727,7 +727,13 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
         d2h = yh.numel() * 4
         n_e2e = e2e_steps
 
+        host_call = not args.hadamard and not args.fused_hadamard and algo == pn.ALGO_AUTO
+
         def e2e_step(i):
+            if host_call:
+                # one C-ABI call: x in from pinned host memory, the GEMVs, y out, wait
+                pn.gemv_layer_host(rot[i % copies], M, xh, yh, ws, stream=stream)
+                return
             x_all.copy_(xh, non_blocking=True)          # every tensor's x (or the rotation's input)
             step(rot[i % copies])
             yh.copy_(y_all[i % copies], non_blocking=True)
@@ -749,8 +755,12 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
         e2e = {"value": world * step_bytes * n_e2e / (e_ms / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "us_per_step": e_ms * 1e3 / n_e2e, "steps": n_e2e,
-               "path": "pinned x -> device (one copy for all tensors), pn_gemv via the Python binding, "
-                       "y -> pinned host (one copy), stream synchronised each step; weights resident"}
+               "path": ("pn_gemv_layer_host through the Python binding: pinned host x -> device (one copy "
+                        "for all tensors), the GEMV launch, y -> pinned host (one copy), stream synchronised, "
+                        "all inside one C-ABI call per step; weights resident") if host_call else
+                       ("pinned x -> device (one copy for all tensors), the rotation and the GEMV via the "
+                        "Python binding, y -> pinned host (one copy), stream synchronised each step; "
+                        "weights resident")}
 
     # read-only ceiling on the same box and buffers: one pn_read_ranges
     # launch per step reads the step's weight copies once (16-byte loads, no

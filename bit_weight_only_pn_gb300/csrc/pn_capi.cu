@@ -327,6 +327,58 @@ pn_status pn_gemv_layer(const pn_gemv_desc* descs, int count, int M, void* works
     return pn_gemv_layer_ex(descs, count, M, workspace, workspace_bytes, PN_ALGO_AUTO, stream);
 }
 
+pn_status pn_gemv_layer_host(const pn_gemv_desc* descs, int count, int M, const uint16_t* x_host, float* y_host,
+                             void* workspace, size_t workspace_bytes, pn_stream stream) {
+    if (!descs || count < 1 || count > PN_MAX_LAYER || !x_host || !y_host) return PN_EINVAL;
+    pn::GemvTensor ts[pn::kMaxLayer];
+    for (int e = 0; e < count; ++e) {
+        const pn_gemv_desc& d = descs[e];
+        pn_status st = check_tensor(d.type, d.W, d.N, d.K, d.x, M, d.y, &ts[e]);
+        if (st != PN_OK) return st;
+    }
+    if (pn_status st = check_layer_overlaps(descs, count, M); st != PN_OK) return st;
+    int sms = 0, major = 0;
+    if (pn_status st = device_info(&sms, &major); st != PN_OK) return st;
+    if (!workspace || !aligned(workspace, 256) || pn::workspace_layout(sms).total > workspace_bytes)
+        return PN_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // one copy per run of entries whose device buffers follow each other (the
+    // host buffers always do)
+    auto copy_runs = [&](bool in) -> cudaError_t {
+        size_t host_off = 0, run_host = 0, run_bytes = 0;
+        uint8_t* run_dev = nullptr;
+        auto flush = [&]() -> cudaError_t {
+            if (!run_bytes) return cudaSuccess;
+            return in ? cudaMemcpyAsync(run_dev, reinterpret_cast<const uint8_t*>(x_host) + run_host, run_bytes,
+                                        cudaMemcpyHostToDevice, s)
+                      : cudaMemcpyAsync(reinterpret_cast<uint8_t*>(y_host) + run_host, run_dev, run_bytes,
+                                        cudaMemcpyDeviceToHost, s);
+        };
+        for (int e = 0; e < count; ++e) {
+            const pn_gemv_desc& d = descs[e];
+            const size_t bytes = in ? static_cast<size_t>(M) * d.K * 2 : static_cast<size_t>(M) * d.N * 4;
+            uint8_t* dev = in ? reinterpret_cast<uint8_t*>(const_cast<uint16_t*>(d.x)) : reinterpret_cast<uint8_t*>(d.y);
+            if (d.N > 0 && bytes > 0) {
+                if (run_bytes && dev == run_dev + run_bytes && host_off == run_host + run_bytes) {
+                    run_bytes += bytes;
+                } else {
+                    if (cudaError_t e2 = flush(); e2 != cudaSuccess) return e2;
+                    run_dev = dev;
+                    run_host = host_off;
+                    run_bytes = bytes;
+                }
+            }
+            host_off += bytes;
+        }
+        return flush();
+    };
+    if (cudaError_t e = copy_runs(true); e != cudaSuccess) return pn::cuda_error(e);
+    if (pn_status st = run_layer(ts, count, M, workspace, workspace_bytes, PN_ALGO_AUTO, s); st != PN_OK) return st;
+    if (cudaError_t e = copy_runs(false); e != cudaSuccess) return pn::cuda_error(e);
+    if (cudaError_t e = cudaStreamSynchronize(s); e != cudaSuccess) return pn::cuda_error(e);
+    return PN_OK;
+}
+
 }  // extern "C"
 
 namespace {

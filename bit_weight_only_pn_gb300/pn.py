@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
             L.pn_gptq_scratch_bytes.argtypes = [i64, i64]
             L.pn_gptq.restype = i32
             L.pn_gptq.argtypes = [i32, vp, i64, i64, vp, i64, ctypes.c_double, vp, vp, sz, vp]
+            L.pn_gemv_layer_host.restype = i32
+            L.pn_gemv_layer_host.argtypes = [ctypes.POINTER(_Desc), i32, i32, vp, vp, vp, sz, vp]
             L.pn_gemv_hadamard.restype = i32
             L.pn_gemv_hadamard.argtypes = [i32, vp, i64, i64, vp, i32, i32, vp, vp, sz, vp]
             L.pn_gemv_layer_hadamard.restype = i32
@@ -237,6 +239,31 @@ def gemv_hadamard(pn_type: int, W: torch.Tensor, K: int, x: torch.Tensor, block:
     _check(lib().pn_gemv_hadamard(pn_type, _ptr(W), N, K, _ptr(x), M, block, _ptr(y), ws_ptr, ws_bytes,
                                   _stream(stream)), "pn_gemv_hadamard")
     return y
+
+
+def gemv_layer_host(entries, M: int, x_host: torch.Tensor, y_host: torch.Tensor, workspace: Workspace,
+                    stream=None) -> torch.Tensor:
+    """pn_gemv_layer_host: x from host memory (every entry's x [M][K] in
+    order, fp16), the GEMVs, y back to host memory (fp32), in one call that
+    returns when y_host is written."""
+    entries = list(entries)
+    if x_host.is_cuda or y_host.is_cuda or x_host.dtype != torch.float16 or y_host.dtype != torch.float32:
+        raise TypeError("x_host must be a CPU float16 tensor and y_host a CPU float32 tensor")
+    if not (x_host.is_contiguous() and y_host.is_contiguous()):
+        raise ValueError("host buffers must be contiguous")
+    need_x = sum(M * K for _, _, K, _, _ in entries)
+    need_y = sum(M * W.shape[0] for _, W, _, _, _ in entries)
+    if x_host.numel() < need_x or y_host.numel() < need_y:
+        raise ValueError("host buffers are too small")
+    arr = (_Desc * len(entries))()
+    for i, (t, W, K, x, y) in enumerate(entries):
+        _require(W, torch.uint8, "W")
+        _require(x, torch.float16, "x")
+        _require(y, torch.float32, "y")
+        arr[i] = _Desc(t, _ptr(W), W.shape[0], K, _ptr(x), _ptr(y))
+    _check(lib().pn_gemv_layer_host(arr, len(entries), M, x_host.data_ptr(), y_host.data_ptr(), workspace.ptr,
+                                    workspace.nbytes, _stream(stream)), "pn_gemv_layer_host")
+    return y_host
 
 
 def gemv_layer_hadamard(entries, M: int, block: int, workspace: Workspace | None = None, stream=None):

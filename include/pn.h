@@ -182,6 +182,22 @@ pn_status pn_gemv_layer_ex(const pn_gemv_desc* descs, int count, int M, void* wo
                            size_t workspace_bytes, int algo, pn_stream stream);
 
 /*
+ * pn_gemv_layer_host: pn_gemv_layer with the activations taken from and the
+ * outputs returned to host memory, end to end in one call.  x_host holds every
+ * entry's x fp16 [M][K] one after the other in entry order, y_host every
+ * entry's y fp32 [M][N] the same way.  The call copies x_host into the
+ * entries' device x buffers, runs the GEMVs (PN_ALGO_AUTO) on `stream`, copies
+ * the entries' device y into y_host and waits for the stream: it returns when
+ * y_host is written.  Entries whose device buffers follow each other are
+ * copied in one transfer.  Page-locked (pinned) host memory keeps the copies
+ * at full speed.  Every check (the descriptors as for pn_gemv_layer, null host
+ * pointers, the workspace, which is required) runs before anything is
+ * enqueued.
+ */
+pn_status pn_gemv_layer_host(const pn_gemv_desc* descs, int count, int M, const uint16_t* x_host, float* y_host,
+                             void* workspace, size_t workspace_bytes, pn_stream stream);
+
+/*
  * pn_gemv_noalloc: pn_gemv for callers that cannot allocate device memory --
  * code running where cudaMalloc is not allowed (a host callback, a stream
  * owned by another runtime), a plugin whose host framework owns every

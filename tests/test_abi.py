@@ -131,6 +131,19 @@ def test_fused_hadamard_checks(lib):
     assert L(arr, 0, 1, 1024, FAKE * 32, 1 << 20, None) == PN_EINVAL
 
 
+def test_layer_host_checks(lib):
+    from bit_weight_only_pn_gb300.pn import _Desc
+    arr = (_Desc * 1)()
+    arr[0] = _Desc(124, FAKE, 32, 5120, FAKE * 2, FAKE * 4)
+    h = lib.pn_gemv_layer_host
+    assert h(arr, 1, 1, None, FAKE * 8, FAKE * 32, 1 << 20, None) == PN_EINVAL          # no host x
+    assert h(arr, 1, 1, FAKE * 8, None, FAKE * 32, 1 << 20, None) == PN_EINVAL          # no host y
+    assert h(arr, 0, 1, FAKE * 8, FAKE * 16, FAKE * 32, 1 << 20, None) == PN_EINVAL     # count
+    assert h(arr, 1, 17, FAKE * 8, FAKE * 16, FAKE * 32, 1 << 20, None) == PN_EINVAL    # M
+    arr[0] = _Desc(124, FAKE, 32, 5120, FAKE * 2 + 1, FAKE * 4)
+    assert h(arr, 1, 1, FAKE * 8, FAKE * 16, FAKE * 32, 1 << 20, None) == PN_EALIGN     # device x
+
+
 def test_gptq_checks(lib):
     # checks that come before any device work
     g = lib.pn_gptq

@@ -339,3 +339,38 @@ def test_cuda_core_staged_layer_and_limits(pn, dev, oracle):
     with pytest.raises(pn.PnError) as err:
         pn.gemv(PN4T, to_dev(W, dev), 65 * 512, to_dev(x, dev), workspace=ws, algo=pn.ALGO_CUDA_CORE_STAGED)
     assert err.value.status == 3
+
+
+def test_layer_host_buffers(pn, dev, oracle):
+    # pn_gemv_layer_host: x from pinned host memory, y back to it, in one call;
+    # device buffers partly contiguous (one copy) and partly apart, with an
+    # empty entry in between
+    from bit_weight_only_pn_gb300 import synth
+    M = 2
+    shapes = [(PN3T, 5120, 300), (PN4T, 6144, 0), (PN4T, 6144, 97), (PN3T, 640, 50)]
+    host_x, host_ref, ents = [], [], []
+    dx = torch.empty(sum(M * K for _, K, _ in shapes[:3]), dtype=torch.float16, device=dev)
+    off = 0
+    for i, (t, K, N) in enumerate(shapes):
+        W = oracle.pack(t, synth.weights(0x7100 + i, max(N, 1), K))[:N]
+        x = synth.activations(0x7200 + i, M, K)
+        host_x.append(x.reshape(-1))
+        if i < 3:
+            xd = dx[off:off + M * K].view(M, K)
+            off += M * K
+        else:
+            xd = torch.empty((M, K), dtype=torch.float16, device=dev)
+        ents.append((t, torch.from_numpy(np.ascontiguousarray(W)).to(dev), K, xd,
+                     torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)))
+        host_ref.append((t, W, K, x, N))
+    xh = torch.from_numpy(np.concatenate(host_x)).pin_memory()
+    yh = torch.full((sum(M * N for _, _, N in shapes),), float("nan"), dtype=torch.float32).pin_memory()
+    ws = pn.Workspace(500, dev)
+    pn.gemv_layer_host(ents, M, xh, yh, ws)
+    assert ws.status() == 0
+    yo = 0
+    for t, W, K, x, N in host_ref:
+        if N:
+            y_ref, abs_sum = oracle.gemv(t, W, K, x)
+            assert_gemv_close(yh[yo:yo + M * N].numpy().reshape(M, N), y_ref, abs_sum)
+        yo += M * N
