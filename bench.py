@@ -728,11 +728,12 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
         n_e2e = e2e_steps
 
         host_call = not args.hadamard and not args.fused_hadamard and algo == pn.ALGO_AUTO
+        calls = [pn.LayerCall(entries, M, ws) for entries in rot] if host_call else None
 
         def e2e_step(i):
             if host_call:
                 # one C-ABI call: x in from pinned host memory, the GEMVs, y out, wait
-                pn.gemv_layer_host(rot[i % copies], M, xh, yh, ws, stream=stream)
+                calls[i % copies].host(xh, yh, stream=stream)
                 return
             x_all.copy_(xh, non_blocking=True)          # every tensor's x (or the rotation's input)
             step(rot[i % copies])
@@ -755,7 +756,8 @@ def measure_gemv(args, cfg, m_override, world, dev, e2e_steps):
         e2e = {"value": world * step_bytes * n_e2e / (e_ms / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "us_per_step": e_ms * 1e3 / n_e2e, "steps": n_e2e,
-               "path": ("pn_gemv_layer_host through the Python binding: pinned host x -> device (one copy "
+               "path": ("pn_gemv_layer_host through the Python binding (pn.LayerCall, arguments marshalled "
+                        "once): pinned host x -> device (one copy "
                         "for all tensors), the GEMV launch, y -> pinned host (one copy), stream synchronised, "
                         "all inside one C-ABI call per step; weights resident") if host_call else
                        ("pinned x -> device (one copy for all tensors), the rotation and the GEMV via the "

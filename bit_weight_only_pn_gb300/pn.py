@@ -241,29 +241,53 @@ def gemv_hadamard(pn_type: int, W: torch.Tensor, K: int, x: torch.Tensor, block:
     return y
 
 
+class LayerCall:
+    """The marshalled arguments of one layer call (pn_gemv_layer /
+    pn_gemv_layer_host) over fixed buffers, built once and reused: a serving
+    loop that calls with the same tensors every step pays one ctypes call per
+    step.  The entries' tensors are kept alive by this object."""
+
+    def __init__(self, entries, M: int, workspace: Workspace):
+        self.entries = list(entries)
+        self.M = M
+        self.workspace = workspace
+        self._arr = (_Desc * len(self.entries))()
+        for i, (t, W, K, x, y) in enumerate(self.entries):
+            _require(W, torch.uint8, "W")
+            _require(x, torch.float16, "x")
+            _require(y, torch.float32, "y")
+            self._arr[i] = _Desc(t, _ptr(W), W.shape[0], K, _ptr(x), _ptr(y))
+        self._n = len(self.entries)
+        self.x_elems = sum(M * K for _, _, K, _, _ in self.entries)
+        self.y_elems = sum(M * W.shape[0] for _, W, _, _, _ in self.entries)
+
+    def device(self, stream=None) -> None:
+        """pn_gemv_layer on the entries' device buffers (enqueued on `stream`)."""
+        _check(lib().pn_gemv_layer(self._arr, self._n, self.M, self.workspace.ptr, self.workspace.nbytes,
+                                   _stream(stream)), "pn_gemv_layer")
+
+    def host(self, x_host: torch.Tensor, y_host: torch.Tensor, stream=None) -> torch.Tensor:
+        """pn_gemv_layer_host: x from host memory, y back to it; returns when
+        y_host is written."""
+        if x_host.is_cuda or y_host.is_cuda or x_host.dtype != torch.float16 or y_host.dtype != torch.float32:
+            raise TypeError("x_host must be a CPU float16 tensor and y_host a CPU float32 tensor")
+        if not (x_host.is_contiguous() and y_host.is_contiguous()):
+            raise ValueError("host buffers must be contiguous")
+        if x_host.numel() < self.x_elems or y_host.numel() < self.y_elems:
+            raise ValueError("host buffers are too small")
+        _check(lib().pn_gemv_layer_host(self._arr, self._n, self.M, x_host.data_ptr(), y_host.data_ptr(),
+                                        self.workspace.ptr, self.workspace.nbytes, _stream(stream)),
+               "pn_gemv_layer_host")
+        return y_host
+
+
 def gemv_layer_host(entries, M: int, x_host: torch.Tensor, y_host: torch.Tensor, workspace: Workspace,
                     stream=None) -> torch.Tensor:
     """pn_gemv_layer_host: x from host memory (every entry's x [M][K] in
     order, fp16), the GEMVs, y back to host memory (fp32), in one call that
-    returns when y_host is written."""
-    entries = list(entries)
-    if x_host.is_cuda or y_host.is_cuda or x_host.dtype != torch.float16 or y_host.dtype != torch.float32:
-        raise TypeError("x_host must be a CPU float16 tensor and y_host a CPU float32 tensor")
-    if not (x_host.is_contiguous() and y_host.is_contiguous()):
-        raise ValueError("host buffers must be contiguous")
-    need_x = sum(M * K for _, _, K, _, _ in entries)
-    need_y = sum(M * W.shape[0] for _, W, _, _, _ in entries)
-    if x_host.numel() < need_x or y_host.numel() < need_y:
-        raise ValueError("host buffers are too small")
-    arr = (_Desc * len(entries))()
-    for i, (t, W, K, x, y) in enumerate(entries):
-        _require(W, torch.uint8, "W")
-        _require(x, torch.float16, "x")
-        _require(y, torch.float32, "y")
-        arr[i] = _Desc(t, _ptr(W), W.shape[0], K, _ptr(x), _ptr(y))
-    _check(lib().pn_gemv_layer_host(arr, len(entries), M, x_host.data_ptr(), y_host.data_ptr(), workspace.ptr,
-                                    workspace.nbytes, _stream(stream)), "pn_gemv_layer_host")
-    return y_host
+    returns when y_host is written.  (LayerCall keeps the marshalled
+    arguments for repeated calls.)"""
+    return LayerCall(entries, M, workspace).host(x_host, y_host, stream)
 
 
 def gemv_layer_hadamard(entries, M: int, block: int, workspace: Workspace | None = None, stream=None):

@@ -374,3 +374,37 @@ def test_layer_host_buffers(pn, dev, oracle):
             y_ref, abs_sum = oracle.gemv(t, W, K, x)
             assert_gemv_close(yh[yo:yo + M * N].numpy().reshape(M, N), y_ref, abs_sum)
         yo += M * N
+
+
+def test_layer_call_reused(pn, dev, oracle):
+    # pn.LayerCall marshals a layer's arguments once; device() and host()
+    # reuse them across calls and steps
+    from bit_weight_only_pn_gb300 import synth
+    M = 1
+    shapes = [(PN3T, 5120, 160), (PN4T, 6144, 77)]
+    ents, refs, xs = [], [], []
+    for i, (t, K, N) in enumerate(shapes):
+        W = oracle.pack(t, synth.weights(0x7300 + i, N, K))
+        x = synth.activations(0x7400 + i, M, K)
+        ents.append((t, torch.from_numpy(W).to(dev), K, torch.from_numpy(x).to(dev),
+                     torch.empty((M, N), dtype=torch.float32, device=dev)))
+        refs.append(oracle.gemv(t, W, K, x))
+        xs.append(x.reshape(-1))
+    call = pn.LayerCall(ents, M, pn.Workspace(237, dev))
+    xh = torch.from_numpy(np.concatenate(xs)).pin_memory()
+    yh = torch.empty(sum(M * N for _, _, N in shapes), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        for e in ents:
+            e[4].fill_(float("nan"))
+        call.device()
+        torch.cuda.synchronize()
+        for e, (y_ref, abs_sum) in zip(ents, refs):
+            assert_gemv_close(e[4].cpu().numpy(), y_ref, abs_sum)
+        yh.fill_(float("nan"))
+        call.host(xh, yh)
+        yo = 0
+        for (t, K, N), (y_ref, abs_sum) in zip(shapes, refs):
+            assert_gemv_close(yh[yo:yo + M * N].numpy().reshape(M, N), y_ref, abs_sum)
+            yo += M * N
+    with pytest.raises(ValueError):
+        call.host(xh[:-1], yh)
