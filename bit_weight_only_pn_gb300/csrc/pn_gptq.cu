@@ -298,7 +298,9 @@ extern "C" pn_status pn_gptq(int type, const float* w, int64_t N, int64_t K, con
                              void* W, void* scratch, size_t scratch_bytes, pn_stream stream) {
     if (type != PN_TYPE_PN3T && type != PN_TYPE_PN4T) return PN_EINVAL;
     const int bpb = pn::per_block(type);
-    if (N < 0 || K <= 0 || K % bpb || n < 1 || !(damp > 0.0) || K > (int64_t(1) << 20)) return PN_EINVAL;
+    // (K x K work is launched as one thread per entry: K at most 65536)
+    if (N < 0 || K <= 0 || K % bpb || n < 1 || !(damp > 0.0) || K > 65536 || N > (int64_t(1) << 34))
+        return PN_EINVAL;
     if (N == 0) return PN_OK;
     if (!w || !X || !W || !scratch) return PN_EINVAL;
     if (reinterpret_cast<uintptr_t>(w) % 4 || reinterpret_cast<uintptr_t>(X) % 4 ||

@@ -279,8 +279,9 @@ pn_status pn_gemv_layer_hadamard(const pn_gemv_desc* descs, int count, int M, in
  * and the rounding), each sum in index order, so the bytes equal the CPU
  * oracle's.  Synchronous (returns when W is written).  scratch: device,
  * 256-byte aligned, pn_gptq_scratch_bytes(N, K) bytes (4 K^2 + N K doubles).
- * w and X 4-byte aligned, W any alignment.  PN_EINVAL for bad sizes, a small
- * scratch, or a Hessian that is not positive definite; N = 0 does nothing.
+ * w and X 4-byte aligned, W any alignment.  K at most 65536.  PN_EINVAL for
+ * bad sizes, a small scratch, or a Hessian that is not positive definite;
+ * N = 0 does nothing.
  * Not part of the GEMV's path: an offline tool, quadratic in K.
  */
 size_t pn_gptq_scratch_bytes(int64_t N, int64_t K);

@@ -164,6 +164,7 @@ def test_gptq_checks(lib):
     assert g(124, FAKE + 2, 8, 160, FAKE * 2, 10, 0.01, FAKE * 4, ws, need, None) == PN_EALIGN
     assert g(124, FAKE, 8, 160, FAKE * 2, 10, 0.01, FAKE * 4, ws + 16, need, None) == PN_EALIGN
     assert g(124, FAKE, 0, 160, FAKE * 2, 10, 0.01, FAKE * 4, ws, need, None) == 0            # nothing to do
+    assert g(125, FAKE, 8, 65600, FAKE * 2, 10, 0.01, FAKE * 4, ws, 1 << 62, None) == PN_EINVAL  # K too wide
 
 
 def test_prefill_checks(lib):
